@@ -1,0 +1,170 @@
+/*
+ * lidx.h -- C ABI of the GB300 (sm_103a) lightning-indexer library, liblidx.so.
+ *
+ * The lightning indexer scores every (query s, compressed key t) pair with
+ *     score[b,s,t] = sum_h w[.,h] * act(q[s,b,h,:] . k[t,b,:])
+ * masks it causally on compressed positions (or with an explicit visibility
+ * tensor), and keeps the top-k keys per query row.  Sources (indexer
+ * documentation pages):
+ *   [P1] "nemo_automodel...deepseek_v4.kernels.tilelang_indexer":
+ *        V4IndexerFunction (layouts q [S,B,H,D] bf16, k [Skv,B,D] bf16,
+ *        weights [S,B,H] fp32; forward(index_q, index_k, weights,
+ *        compress_ratio, topk, topk_indices=None); backward(grad_scores,
+ *        grad_indices)), v4_lighting_indexer (returns [B,S,topk] fp32),
+ *        pytorch_extract_topk_scores(logits, topk_indices).
+ *   [P2] "nemo_automodel...deepseek_v4.kernels.tilelang_indexer_fwd":
+ *        _make_causal_cu_seqlens (query p sees groups [0,(p+1)//compress_ratio)),
+ *        batched_indexer_fwd / indexer_fwd_interface ([S,Skv] fp32 logits over
+ *        cu_seqlen_ks..cu_seqlen_ke, clean_logits=True), clean_logits_.
+ *   [P3] "nemo_automodel...deepseek_v41.indexer": indexer_scores(queries
+ *        [B,S,H,D] bf16, keys [B,Skv,D] bf16, weights [B,S,H] bf16, allowed
+ *        [B,S,Skv] bool) -> bf16 [B,S,Skv]; GEMM result and weighted head score
+ *        rounded to bf16 before an fp32 head reduction.
+ *
+ * Conventions for every call:
+ *   - Pointers are DEVICE pointers on the current CUDA device unless the
+ *     argument says "host".  The caller owns every buffer; the library never
+ *     allocates device memory (its only device state is a file-scope status
+ *     word).  Inputs are read-only; outputs are fully overwritten (padding
+ *     included) unless stated.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and returns without synchronising.  A nonzero return means
+ *     nothing was launched, except LIDX_ERR_CUDA (a launch failed).
+ *   - Argument rules (checked before any launch, LIDX_ERR_SHAPE otherwise):
+ *     H a power of two <= 128 and D a multiple of 16 [P3 queries parameter],
+ *     here also D <= 128; B, S >= 1; Skv >= 0; compress_ratio >= 1; topk >= 1
+ *     where a top-k is asked for.  Base pointers of bf16/fp32 tensors must be
+ *     16-byte aligned (LIDX_ERR_ALIGN); tensors are dense and contiguous in the
+ *     stated layout.  NULL where a buffer is required -> LIDX_ERR_NULL.
+ *   - Inputs must be finite; NaN or inf inputs give unspecified (but
+ *     in-bounds) results.
+ *   - Device-side failures (a pipeline wait that exceeds its time limit) are
+ *     recorded in the status word read by lidx_device_status().
+ */
+#ifndef LIDX_H
+#define LIDX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LIDX_OK = 0,
+    LIDX_ERR_NULL = 1,        /* required pointer is NULL */
+    LIDX_ERR_SHAPE = 2,       /* size/shape rule violated */
+    LIDX_ERR_ALIGN = 3,       /* pointer not 16-byte aligned */
+    LIDX_ERR_UNSUPPORTED = 4, /* valid request outside what this build implements */
+    LIDX_ERR_WORKSPACE = 5,   /* workspace too small (see lidx_workspace_bytes) */
+    LIDX_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed */
+    LIDX_ERR_DEVICE_TIMEOUT = 7, /* a kernel gave up on a pipeline wait */
+    LIDX_ERR_NO_DEVICE = 8    /* no sm_103a device current */
+} lidx_status;
+
+typedef enum { LIDX_ACT_RELU = 0, LIDX_ACT_IDENTITY = 1 } lidx_act;
+
+/* Operation ids for lidx_workspace_bytes. */
+typedef enum { LIDX_OP_INDEXER_FWD = 0, LIDX_OP_INDEXER_BWD = 1, LIDX_OP_SCORES_V41 = 2 } lidx_op;
+
+/*
+ * V4 forward: causal mask + per-row top-k   [P1 V4IndexerFunction.forward,
+ * v4_lighting_indexer; P2 _make_causal_cu_seqlens].
+ *   q  bf16 [S,B,H,D]   k bf16 [Skv,B,D]   w fp32 [S,B,H]   (SBHD, row-major)
+ *   Row (b,s) sees keys t in [0, min((s+1)/compress_ratio, Skv)).
+ *   logits_out  fp32 [B,S,Skv], nullable.  Non-NULL: every entry is written,
+ *               masked ones as -inf, and the top-k reads it back.  NULL: the
+ *               logits are never written to HBM (fused path; needs workspace).
+ *   topk_indices_in  int32 [B,S,topk], nullable.  Non-NULL: no selection; the
+ *               scores of the given indices are returned (entries outside the
+ *               row's visible range give -inf) and indices_out is a copy.
+ *   indices_out int32 [B,S,topk]  scores_out fp32 [B,S,topk]: sorted by score
+ *               descending, equal scores by ascending index; rows with fewer
+ *               than topk visible keys end with index -1 / score -inf.
+ *   workspace   device scratch of lidx_workspace_bytes(LIDX_OP_INDEXER_FWD,..)
+ *               bytes (may be NULL when that is 0), 256-byte aligned.
+ *   Limits of this build: Skv <= 4096 when a selection is made.
+ */
+int lidx_indexer_fwd(const void* q, const void* k, const float* w,
+                     int64_t B, int64_t S, int64_t Skv, int H, int D,
+                     int compress_ratio, int topk, int act,
+                     const int32_t* topk_indices_in, float* logits_out,
+                     int32_t* indices_out, float* scores_out,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Logits only, explicit ranges   [P2 batched_indexer_fwd, indexer_fwd_interface,
+ * clean_logits_].  Same layouts as lidx_indexer_fwd.
+ *   ks, ke  int32 [S] (device), nullable together: NULL -> causal ranges from
+ *           compress_ratio.  Row (b,s) sees t in [max(ks[s],0), min(ke[s],Skv)).
+ *   clean   1: entries outside the range are -inf.  0: entries outside the
+ *           range are unspecified (left as they were or holding raw scores).
+ *   logits_out fp32 [B,S,Skv].
+ */
+int lidx_indexer_logits(const void* q, const void* k, const float* w,
+                        int64_t B, int64_t S, int64_t Skv, int H, int D,
+                        int compress_ratio, const int32_t* ks, const int32_t* ke,
+                        int clean, int act, float* logits_out, void* stream);
+
+/*
+ * Gather at indices   [P1 pytorch_extract_topk_scores(logits, topk_indices)].
+ *   logits fp32 [B,S,Skv]; idx int32 [B,S,topk]; scores_out fp32 [B,S,topk] =
+ *   logits[b,s,idx], -inf where idx is outside [0,Skv).  Bit-exact copy.
+ */
+int lidx_extract_topk_scores(const float* logits, const int32_t* idx,
+                             int64_t B, int64_t S, int64_t Skv, int topk,
+                             float* scores_out, void* stream);
+
+/*
+ * V4.1 scores   [P3 indexer_scores, module docstring].
+ *   q bf16 [B,S,H,D]  k bf16 [B,Skv,D]  w bf16 [B,S,H]  allowed u8/bool [B,S,Skv]
+ *   scores_out bf16 [B,S,Skv]: where allowed[b,s,t] != 0,
+ *       bf16( sum_h  bf16( act(bf16(q.k)) * w ) )   (fp32 head reduction),
+ *   and -inf (0xFF80) elsewhere.  allowed needs no alignment.
+ *   workspace: lidx_workspace_bytes(LIDX_OP_SCORES_V41, ...) bytes.
+ */
+int lidx_indexer_scores_v41(const void* q, const void* k, const void* w,
+                            const uint8_t* allowed, int64_t B, int64_t S, int64_t Skv,
+                            int H, int D, int act, void* scores_out,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * V4 backward through the selected entries   [P1 V4IndexerFunction.backward;
+ * grad_indices carries no gradient and is not an argument].
+ *   idx int32 [B,S,topk] (as returned by the forward), grad_scores fp32
+ *   [B,S,topk].  Slots with idx outside the row's causal range (padding -1
+ *   included) contribute nothing.  For every other slot, with t = idx,
+ *   g = grad, x = q[s,b,h,:].k[t,b,:]:
+ *     dw[s,b,h] += g*act(x);  dq[s,b,h,:] += g*w*act'(x)*k[t,b,:];
+ *     dk[t,b,:] += sum_h g*w*act'(x)*q[s,b,h,:]        (ReLU'(0) = 0)
+ *   dq fp32 [S,B,H,D], dk fp32 [Skv,B,D], dw fp32 [S,B,H]; all overwritten.
+ *   grad_dtype must be 0 (fp32 outputs) in this build.
+ *   workspace: lidx_workspace_bytes(LIDX_OP_INDEXER_BWD, ...) bytes.
+ */
+int lidx_indexer_bwd(const void* q, const void* k, const float* w,
+                     const int32_t* idx, const float* grad_scores,
+                     int64_t B, int64_t S, int64_t Skv, int H, int D,
+                     int compress_ratio, int topk, int act, int grad_dtype,
+                     void* dq, void* dk, float* dw,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* Device scratch the call needs for these sizes, in bytes (0 = none).
+ * logits_materialised: 1 if logits_out will be non-NULL (LIDX_OP_INDEXER_FWD). */
+size_t lidx_workspace_bytes(int op, int64_t B, int64_t S, int64_t Skv, int H, int D,
+                            int topk, int logits_materialised);
+
+/* Synchronises `stream`, returns the device status word (LIDX_OK or
+ * LIDX_ERR_DEVICE_TIMEOUT) and clears it.  LIDX_ERR_CUDA if the sync fails. */
+int lidx_device_status(void* stream);
+
+/* Static English description of a status code (never NULL). */
+const char* lidx_status_string(int status);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int lidx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LIDX_H */

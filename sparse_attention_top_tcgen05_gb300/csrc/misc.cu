@@ -1,0 +1,41 @@
+// misc.cu -- small memory-bound kernels: gather of scores at given indices
+// ("tilelang_indexer" page, pytorch_extract_topk_scores(logits, topk_indices)).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace lidx {
+
+// One thread per output element; consecutive threads read consecutive
+// indices (coalesced) and gather from the row's logits (L2-friendly).
+__global__ void extract_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx,
+                               int64_t rows, int64_t Skv, int topk, float* __restrict__ out) {
+    const int64_t n = rows * (int64_t)topk;
+    const float ninf = __int_as_float(0xff800000);
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = e / topk;
+        const int32_t t = idx[e];
+        out[e] = (t >= 0 && t < Skv) ? logits[r * Skv + t] : ninf;
+    }
+}
+
+cudaError_t extract_launch(const float* logits, const int32_t* idx, int64_t rows, int64_t Skv,
+                           int topk, float* out, cudaStream_t stream) {
+    const int64_t n = rows * (int64_t)topk;
+    if (n == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t blocks = (n + 255) / 256;
+    const int64_t cap = (int64_t)sms * 8;
+    if (blocks > cap) blocks = cap;
+    extract_kernel<<<(unsigned)blocks, 256, 0, stream>>>(logits, idx, rows, Skv, topk, out);
+    return cudaGetLastError();
+}
+
+LIDX_STATUS_READER(status_misc)
+
+}  // namespace lidx

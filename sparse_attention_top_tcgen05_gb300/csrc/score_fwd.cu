@@ -1,0 +1,428 @@
+// score_fwd.cu -- V4 lightning-indexer forward on sm_103a tensor cores.
+//
+// Computes, for a tile of query rows against every visible compressed key,
+//     logit[b,s,t] = sum_h w[s,b,h] * act(q[s,b,h,:] . k[t,b,:])
+// ("tilelang_indexer" page, V4IndexerFunction: SBHD layouts; "tilelang_indexer_fwd"
+// page, batched_indexer_fwd / indexer_fwd_interface / clean_logits_ /
+// _make_causal_cu_seqlens), then optionally the per-row top-k.
+//
+// Design (one persistent CTA per SM, warp-specialised):
+//   * The contraction is oriented keys x (query, head): UMMA M = 128 keys,
+//     N = 256 columns = QT queries x H heads, K = D.  Each TMEM lane is one key,
+//     so the head reduction sum_h w*act(x) is a per-thread loop over columns
+//     with no cross-lane traffic, and logits stores are 128 consecutive keys.
+//   * warp 0 lane 0: TMA producer.  The query tile [QT*H rows, D] stays resident
+//     for the whole key sweep; key tiles [128, D] stream through a 3-stage ring.
+//   * warp 1 lane 0: tcgen05.mma issuer into two 256-column fp32 accumulators
+//     (512 TMEM columns), so the MMA of tile i+1 overlaps the epilogue of tile i.
+//   * warps 2..9: epilogue.  tcgen05.ld -> act -> weighted head sum in fp32 ->
+//     mask -> store (logits) or stash in a per-CTA L2-resident row buffer.
+//     After the query tile's sweep the same 256 threads run the top-k of its
+//     rows (topk.cuh).
+//   * Key tiles past the tile's last visible key are never loaded or multiplied.
+//     Query tiles are dealt to CTAs heaviest-first in a snake order.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "topk.cuh"
+
+namespace lidx {
+
+constexpr int kN = 256;            // UMMA N: query x head columns per tile
+constexpr int kM = 128;            // UMMA M: keys per tile
+constexpr int kStages = 3;         // key-tile ring depth
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kEpiBar = 1;         // named barrier id of the epilogue group
+
+struct Unit {
+    int b, s0;
+    int lo_t, hi_t;  // key tiles [lo_t, hi_t) with work
+    int lo_k, hi_k;  // visible keys of the tile's union range
+};
+
+__device__ __forceinline__ void row_range(const ScoreParams& p, int s, int& lo, int& hi) {
+    if (p.ks == nullptr) {
+        lo = 0;
+        long long e = (long long)(s + 1) / p.ratio;
+        hi = (int)(e < p.Skv ? e : p.Skv);
+    } else {
+        lo = p.ks[s] > 0 ? p.ks[s] : 0;
+        hi = p.ke[s] < p.Skv ? p.ke[s] : p.Skv;
+        if (hi < lo) hi = lo;
+    }
+}
+
+template <int QT>
+__device__ __forceinline__ Unit make_unit(const ScoreParams& p, int u) {
+    Unit un;
+    const int qt = p.qtiles - 1 - u / p.B;  // heaviest (latest) query tiles first
+    un.b = u % p.B;
+    un.s0 = qt * QT;
+    const int s_last = min(un.s0 + QT - 1, p.S - 1);
+    if (p.ks == nullptr) {
+        int lo, hi;
+        row_range(p, s_last, lo, hi);
+        un.lo_k = 0;
+        un.hi_k = hi;
+    } else {
+        int lo = p.Skv, hi = 0;
+        for (int s = un.s0; s <= s_last; ++s) {
+            int a, e;
+            row_range(p, s, a, e);
+            if (e > a) {
+                lo = min(lo, a);
+                hi = max(hi, e);
+            }
+        }
+        un.lo_k = lo;
+        un.hi_k = hi;
+    }
+    if (un.hi_k > un.lo_k) {
+        un.lo_t = un.lo_k / kM;
+        un.hi_t = (un.hi_k + kM - 1) / kM;
+    } else {
+        un.lo_t = un.hi_t = 0;
+    }
+    return un;
+}
+
+// i-th unit of this CTA in snake order, or -1 when past the end
+__device__ __forceinline__ int unit_of(int i, int num_units) {
+    const int G = gridDim.x;
+    const int base = i * G;
+    if (base >= num_units) return -2;
+    const int u = base + ((i & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+    return u < num_units ? u : -1;
+}
+
+__device__ __forceinline__ float act_f(float x, int act) { return act == 0 ? fmaxf(x, 0.f) : x; }
+
+struct SmemLayout {
+    uint32_t q_off, k_off, w_off, range_off, topk_off, bar_off, tmem_off, total;
+};
+
+__host__ __device__ inline SmemLayout smem_layout(int D) {
+    SmemLayout L;
+    uint32_t o = 0;
+    L.q_off = o;
+    o += kN * D * 2;
+    L.k_off = o;
+    o += kStages * kM * D * 2;
+    L.w_off = o;
+    o += kN * 4;
+    L.range_off = o;
+    o += 2 * kN * 4;
+    L.topk_off = o;
+    o += (uint32_t)((sizeof(TopkSmem) + 15) / 16 * 16);
+    L.bar_off = o;
+    o += 16 * 8;
+    L.tmem_off = o;
+    o += 16;
+    L.total = o + 1024;  // slack for 1024-byte alignment of the base
+    return L;
+}
+
+template <int H>
+__global__ void __launch_bounds__(kThreads, 1)
+    score_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                     const ScoreParams p) {
+    constexpr int QT = kN / H;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const SmemLayout L = smem_layout(p.D);
+    uint8_t* sQ = smem + L.q_off;
+    uint8_t* sK = smem + L.k_off;
+    float* sW = (float*)(smem + L.w_off);
+    int* sLo = (int*)(smem + L.range_off);
+    int* sHi = sLo + kN;
+    TopkSmem& sT = *(TopkSmem*)(smem + L.topk_off);
+    uint64_t* bars = (uint64_t*)(smem + L.bar_off);
+    uint64_t* q_full = bars + 0;
+    uint64_t* q_empty = bars + 1;
+    uint64_t* k_full = bars + 2;              // [kStages]
+    uint64_t* k_empty = bars + 2 + kStages;   // [kStages]
+    uint64_t* acc_full = bars + 2 + 2 * kStages;  // [2]
+    uint64_t* acc_empty = acc_full + 2;           // [2]
+    uint32_t* tmem_slot = (uint32_t*)(smem + L.tmem_off);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int swz = p.swz, KB = swz / 2, nkb = p.D / KB;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(k_full + i, 1);
+            mbar_init(k_empty + i, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(acc_full + i, 1);
+            mbar_init(acc_empty + i, kEpiWarps);
+        }
+        fence_mbar_init();
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int kcount = 0, qcount = 0;
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                const int u = unit_of(i, p.num_units);
+                if (u == -2) break;
+                if (u < 0) continue;
+                const Unit un = make_unit<QT>(p, u);
+                if (un.hi_t <= un.lo_t) continue;
+                if (!(ok = mbar_wait(q_empty, (qcount & 1) ^ 1))) break;
+                ++qcount;
+                mbar_arrive_expect_tx(q_full, kN * p.D * 2);
+                for (int kb = 0; kb < nkb; ++kb)
+                    tma_load_4d(sQ + kb * kN * swz, &tmq, q_full, kb * KB, 0, un.b, un.s0);
+                for (int kt = un.lo_t; kt < un.hi_t; ++kt, ++kcount) {
+                    const int st = kcount % kStages;
+                    if (!(ok = mbar_wait(k_empty + st, ((kcount / kStages) & 1) ^ 1))) break;
+                    uint8_t* dst = sK + st * kM * p.D * 2;
+                    mbar_arrive_expect_tx(k_full + st, kM * p.D * 2);
+                    for (int kb = 0; kb < nkb; ++kb)
+                        tma_load_3d(dst + kb * kM * swz, &tmk, k_full + st, kb * KB, un.b, kt * kM);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kM, kN);
+            int kcount = 0, tcount = 0, qcount = 0;
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                const int u = unit_of(i, p.num_units);
+                if (u == -2) break;
+                if (u < 0) continue;
+                const Unit un = make_unit<QT>(p, u);
+                if (un.hi_t <= un.lo_t) continue;
+                if (!(ok = mbar_wait(q_full, qcount & 1))) break;
+                ++qcount;
+                tc_fence_after();
+                for (int kt = un.lo_t; kt < un.hi_t; ++kt, ++kcount, ++tcount) {
+                    const int st = kcount % kStages, acc = tcount & 1;
+                    if (!(ok = mbar_wait(acc_empty + acc, ((tcount >> 1) & 1) ^ 1))) break;
+                    tc_fence_after();
+                    if (!(ok = mbar_wait(k_full + st, (kcount / kStages) & 1))) break;
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sK + st * kM * p.D * 2);
+                    const uint32_t b0 = smem_u32(sQ);
+                    const uint32_t d = tmem_base + acc * kN;
+                    for (int k = 0; k < p.D / 16; ++k) {
+                        const int kb = (k * 16) / KB, koff = ((k * 16) % KB) * 2;
+                        const uint64_t ad = smem_desc_kmajor(a0 + kb * kM * swz + koff, swz);
+                        const uint64_t bd = smem_desc_kmajor(b0 + kb * kN * swz + koff, swz);
+                        umma_f16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+                    }
+                    umma_commit(k_empty + st);
+                    umma_commit(acc_full + acc);
+                }
+                if (ok) umma_commit(q_empty);
+            }
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int etid = threadIdx.x - 64;
+        const int quad = warp & 3;           // TMEM lane quadrant this warp may read
+        const int half = (warp - 2) >> 2;    // which 128 of the 256 columns
+        const int row_t = quad * 32 + lane;  // key within the tile
+        constexpr int QH = QT / 2;           // queries per half (H <= 128)
+        const float ninf = __int_as_float(0xff800000);
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
+        const int ntiles_all = (p.Skv + kM - 1) / kM;
+        const bool materialise = p.logits != nullptr;
+        int tcount = 0;
+        bool ok = true;
+        float* scratch = p.scratch ? p.scratch + (size_t)blockIdx.x * p.scratch_stride_cta : nullptr;
+        for (int i = 0; ok; ++i) {
+            const int u = unit_of(i, p.num_units);
+            if (u == -2) break;
+            if (u < 0) continue;
+            const Unit un = make_unit<QT>(p, u);
+            named_bar_sync(kEpiBar, kEpiThreads);
+            for (int e = etid; e < kN; e += kEpiThreads) {
+                const int ql = e / H, h = e % H, s = un.s0 + ql;
+                sW[e] = s < p.S ? p.w[((size_t)s * p.B + un.b) * H + h] : 0.f;
+            }
+            for (int ql = etid; ql < QT; ql += kEpiThreads) {
+                const int s = un.s0 + ql;
+                int lo = 0, hi = -1;  // hi < 0: no such query row
+                if (s < p.S) row_range(p, s, lo, hi);
+                sLo[ql] = lo;
+                sHi[ql] = hi;
+            }
+            named_bar_sync(kEpiBar, kEpiThreads);
+            const int t_begin = materialise ? 0 : un.lo_t;
+            const int t_end = materialise ? ntiles_all : un.hi_t;
+            const float* wh = sW + half * 128;
+            for (int kt = t_begin; kt < t_end; ++kt) {
+                const int t = kt * kM + row_t;
+                const bool computed = kt >= un.lo_t && kt < un.hi_t;
+                if (!computed) {
+                    // tile outside every row's range: masked fill only
+                    if (p.clean && t < p.Skv)
+                        for (int j = 0; j < QH; ++j) {
+                            const int ql = half * QH + j;
+                            if (sHi[ql] >= 0)
+                                p.logits[((size_t)un.b * p.S + un.s0 + ql) * p.Skv + t] = ninf;
+                        }
+                    continue;
+                }
+                const int acc = tcount & 1;
+                if (!(ok = mbar_wait(acc_full + acc, (tcount >> 1) & 1))) break;
+                ++tcount;
+                tc_fence_after();
+                // this half's 128 accumulator columns, as 4 chunks of 32
+                uint32_t r[4][32];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + acc * kN + (half * 4 + c) * 32, r[c]);
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty + acc);  // accumulator may be reused
+                float run = 0.f;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int cih = c * 32 + jj;  // column within the half (compile time)
+                        const int j = cih / H, h = cih % H;
+                        const float x = __uint_as_float(r[c][jj]);
+                        run = fmaf(wh[cih], act_f(x, p.act), h == 0 ? 0.f : run);
+                        if (h == H - 1) {
+                            const int ql = half * QH + j;
+                            const int lo = sLo[ql], hi = sHi[ql];
+                            if (hi >= 0) {
+                                const bool vis = t >= lo && t < hi;
+                                if (materialise) {
+                                    if (t < p.Skv && (vis || p.clean))
+                                        p.logits[((size_t)un.b * p.S + un.s0 + ql) * p.Skv + t] =
+                                            vis ? run : ninf;
+                                } else {
+                                    scratch[(size_t)ql * p.Skv_pad + t] = run;
+                                }
+                            }
+                        }
+                    }
+                }
+            }
+            if (!ok) break;
+            if (p.topk > 0) {
+                named_bar_sync(kEpiBar, kEpiThreads);  // row buffers complete and visible
+                for (int ql = 0; ql < QT; ++ql) {
+                    const int s = un.s0 + ql;
+                    if (s >= p.S) break;
+                    const int lo = sLo[ql], hi = sHi[ql];
+                    const size_t orow = ((size_t)un.b * p.S + s) * p.topk;
+                    const float* row = materialise ? p.logits + ((size_t)un.b * p.S + s) * p.Skv
+                                                   : scratch + (size_t)ql * p.Skv_pad;
+                    row_topk<kEpiThreads>(row, lo, hi, p.topk, p.out_idx + orow, p.out_sc + orow, sT,
+                                          etid, kEpiBar);
+                }
+            }
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+// ------------------------------------------------------------------- host
+LIDX_STATUS_READER(status_score_fwd)
+
+static int encode_maps(const ScoreLaunch& a, CUtensorMap* mq, CUtensorMap* mk) {
+    const int swz = a.p.swz, KB = swz / 2;
+    const CUtensorMapSwizzle sw = swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swz == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+    const int H = a.p.H, D = a.p.D, B = a.p.B;
+    const int QT = kN / H;
+    // q [S,B,H,D]: dims (D, H, B, S)
+    cuuint64_t qdim[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)B, (cuuint64_t)a.p.S};
+    cuuint64_t qstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)B * H * D * 2};
+    cuuint32_t qbox[4] = {(cuuint32_t)KB, (cuuint32_t)H, 1, (cuuint32_t)QT};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    if (encode_tiled(mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void*)a.q, qdim, qstr, qbox, es, sw))
+        return 1;
+    // k [Skv,B,D]: dims (D, B, Skv)
+    cuuint64_t kdim[3] = {(cuuint64_t)D, (cuuint64_t)B, (cuuint64_t)(a.p.Skv > 0 ? a.p.Skv : 1)};
+    cuuint64_t kstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)B * D * 2};
+    cuuint32_t kbox[3] = {(cuuint32_t)KB, 1, (cuuint32_t)kM};
+    if (encode_tiled(mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.k, kdim, kstr, kbox, es, sw))
+        return 1;
+    return 0;
+}
+
+template <int H>
+static cudaError_t launch_h(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                            int smem, int grid) {
+    auto kern = score_fwd_kernel<H>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, a.p);
+    return cudaGetLastError();
+}
+
+size_t score_scratch_bytes(int64_t S, int64_t Skv, int H, int num_sms) {
+    (void)S;
+    const int QT = kN / H;
+    const int64_t Skv_pad = (Skv + kM - 1) / kM * kM;
+    return (size_t)num_sms * QT * Skv_pad * sizeof(float);
+}
+
+int score_fwd_launch(ScoreLaunch& a) {
+    ScoreParams& p = a.p;
+    const int QT = kN / p.H;
+    p.swz = (p.D % 64 == 0) ? 128 : (p.D % 32 == 0 ? 64 : 32);
+    p.qtiles = (p.S + QT - 1) / QT;
+    p.num_units = p.B * p.qtiles;
+    p.Skv_pad = (p.Skv + kM - 1) / kM * kM;
+    p.scratch_stride_cta = (int64_t)QT * p.Skv_pad;
+    const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+    if (grid <= 0) return 0;
+    CUtensorMap mq, mk;
+    if (encode_maps(a, &mq, &mk)) return -1;
+    // at least 120 KB so that one CTA (and its 512 TMEM columns) owns each SM
+    int smem = (int)smem_layout(p.D).total;
+    if (smem < 120 * 1024) smem = 120 * 1024;
+    cudaError_t e;
+    switch (p.H) {
+        case 1: e = launch_h<1>(a, mq, mk, smem, grid); break;
+        case 2: e = launch_h<2>(a, mq, mk, smem, grid); break;
+        case 4: e = launch_h<4>(a, mq, mk, smem, grid); break;
+        case 8: e = launch_h<8>(a, mq, mk, smem, grid); break;
+        case 16: e = launch_h<16>(a, mq, mk, smem, grid); break;
+        case 32: e = launch_h<32>(a, mq, mk, smem, grid); break;
+        case 64: e = launch_h<64>(a, mq, mk, smem, grid); break;
+        case 128: e = launch_h<128>(a, mq, mk, smem, grid); break;
+        default: return -2;
+    }
+    a.launched = grid;
+    return e == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace lidx
