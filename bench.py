@@ -1,0 +1,397 @@
+"""Benchmark of the lightning-indexer hot path on one GB300 (or N replicas).
+
+Headline: the fused long-context V4 forward (score + causal mask + top-k,
+logits never written) at B=2, S=16384, H=64, D=128, compress_ratio 4
+(Skv=4096), topk=2048, bf16 inputs, fp32 accumulation.
+
+  value  = valid-pair TFLOP/s = (visible causal pairs x 2*H*D) / step time,
+           inputs resident in HBM (q alone is 537 MB, larger than the 129 MB L2)
+  e2e    = the same metric through the C ABI with host buffers: pinned
+           host->device copy of q, k, w and device->host copy of indices and
+           scores inside the timed region
+  roofline: the scoring kernel against the measured dense bf16 peak
+  cpu_baseline: the CPU oracle on a strided sample of the same rows
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs one replica; rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SCORE_SRC = ["sparse_attention_top_tcgen05_gb300/csrc/score_fwd.cu",
+             "sparse_attention_top_tcgen05_gb300/csrc/topk.cuh",
+             "sparse_attention_top_tcgen05_gb300/csrc/ptx.cuh"]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def src_hash(paths):
+    h = hashlib.sha256()
+    for rel in paths:
+        h.update(open(os.path.join(ROOT, rel), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key, paths):
+    """dram bytes per launch from a committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel_key)
+    if not d or d.get("src_hash") != src_hash(paths):
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+def visible_pairs(S, Skv, ratio, B):
+    s = np.arange(S, dtype=np.int64)
+    return int(np.minimum((s + 1) // ratio, Skv).sum()) * B
+
+
+class Clocks:
+    """nvidia-smi sampler running while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(wl, stride, seed=0):
+    """Time the oracle (as it stands) on every `stride`-th row of the workload."""
+    import oracle
+
+    q, k, w = workloads.v4_inputs(wl, seed)
+    rows = workloads.sample_rows(wl.B, wl.S, stride, 0)
+    ks, ke = oracle.causal_ranges(wl.S, wl.Skv, wl.ratio)
+    pairs = int(sum(ke[r % wl.S] - ks[r % wl.S] for r in rows))
+    t0 = time.perf_counter()
+    oracle.indexer_fwd_rows(q, k, w, wl.ratio, wl.topk, rows=rows)
+    dt = time.perf_counter() - t0
+    flops = pairs * 2.0 * wl.H * wl.D
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.get_threads(),
+            "kind": "oracle", "rows_per_s": len(rows) / dt, "seconds": dt,
+            "sample": f"{len(rows)} query rows (every {stride}th row of each batch plus the last), "
+                      f"{pairs} visible pairs, full fp64 logits + top-k per row"}
+
+
+def run_reference(args, wl, world, rank):
+    if rank != 0:
+        return
+    steps = []
+    stride = 64
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, stride * 4)
+    for _ in range(args.steps):
+        steps.append(cpu_oracle_sample(wl, stride))
+    v = statistics.median(s["value"] for s in steps)
+    cb = dict(steps[0])
+    cb["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * statistics.median(s["seconds"] for s in steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_of(wl, 1),
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+METRIC = "indexer valid-pair TFLOP/s and query-rows/s incl. top-k; % of GB300 BF16 peak"
+
+
+def config_of(wl, n):
+    return {"workload": f"{wl.name}: V4 fused score+causal mask+top-k, logits not materialised",
+            "B": wl.B, "S": wl.S, "H": wl.H, "D": wl.D, "Skv": wl.Skv,
+            "compress_ratio": wl.ratio, "topk": wl.topk, "act": "relu",
+            "inputs": "bf16 q,k ~N(0,1/D); fp32 w ~N(0,1/H); seed 0",
+            "l2": "inputs larger than L2 (q = 537 MB > 129 MB), no flush",
+            "parallelism": f"replicas x{n}"}
+
+
+# ------------------------------------------------------------------- GPU arm
+def time_steps(fn, steps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def side_workloads(lidx, pk):
+    """Short measurements of the other workloads' kernels (not the headline)."""
+    out = {}
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    wl = workloads.WORKLOADS["c4_fwd"]
+    q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
+    idx = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.int32, device="cuda")
+    sc = torch.empty_like(idx, dtype=torch.float32)
+    lg = torch.empty(wl.B, wl.S, wl.Skv, dtype=torch.float32, device="cuda")
+    fn = lambda: lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk, materialise_logits=True,
+                                       out=(idx, sc, lg))
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(10):
+        flush.zero_()
+        ts.append(time_steps(fn, 1, stream))
+    ms = statistics.median(ts)
+    pairs = visible_pairs(wl.S, wl.Skv, wl.ratio, wl.B)
+    fl = pairs * 2.0 * wl.H * wl.D
+    alg_bytes = q.numel() * 2 + k.numel() * 2 + w.numel() * 4 + lg.numel() * 4 + idx.numel() * 8
+    out["c4_fwd"] = {"ms": ms, "tflops": fl / ms / 1e9, "rows_per_s": wl.B * wl.S / ms * 1e3,
+                     "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
+                     "hbm_gbs": alg_bytes / ms / 1e6, "hbm_frac": alg_bytes / ms / 1e6 / pk["hbm_gbs"],
+                     "l2": "256 MB flush before each launch"}
+    del q, k, w, idx, sc, lg
+    return out
+
+
+def run_gpu(args, wl, world, rank, local):
+    import sparse_attention_top_tcgen05_gb300 as lidx
+
+    pk, pk_src = peaks()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    q, k, w = workloads.v4_inputs(wl, args.seed + rank)
+    qd, kd, wd = q.to(dev), k.to(dev), w.to(dev)
+    B, S, H, D, Skv, topk = wl.B, wl.S, wl.H, wl.D, wl.Skv, wl.topk
+    idx = torch.empty(B, S, topk, dtype=torch.int32, device=dev)
+    sc = torch.empty(B, S, topk, dtype=torch.float32, device=dev)
+    ws_bytes = lidx.lidx_workspace_bytes(lidx.OP_INDEXER_FWD, B, S, Skv, H, D, topk, False)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        lidx.lidx_indexer_fwd(qd, kd, wd, wl.ratio, topk, out=(idx, sc, None), workspace=ws)
+
+    pairs = visible_pairs(S, Skv, wl.ratio, B)
+    flops = pairs * 2.0 * H * D
+    launches_per_step = 1
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert lidx.lidx_device_status() == 0
+    barrier(world)
+    with Clocks(local) as clk:
+        torch.cuda.synchronize()
+        ms = time_steps(step, args.steps, stream)
+        torch.cuda.synchronize()
+    barrier(world)
+    status = lidx.lidx_device_status()
+    ms_max = max_over_ranks(ms, world)
+    value = world * flops / (ms_max * 1e-3) / 1e12
+    rows_per_s = world * B * S / (ms_max * 1e-3)
+
+    if args.no_e2e:
+        e2e_ms = float("nan")
+    else:
+        e2e_ms = e2e_measure(q, k, w, qd, kd, wd, idx, sc, step, args, world, stream)
+    h2d = q.numel() * 2 + k.numel() * 2 + w.numel() * 4
+    d2h = idx.numel() * 4 + sc.numel() * 4
+
+    if rank != 0:
+        return
+    emit(args, wl, world, ms, ms_max, flops, pairs, value, rows_per_s, e2e_ms, h2d, d2h,
+         launches_per_step, clk, status, pk, pk_src, lidx)
+
+
+def e2e_measure(q, k, w, qd, kd, wd, idx, sc, step, args, world, stream):
+    """Same step through the C ABI with host buffers: pinned H2D inputs, D2H outputs."""
+    qh, kh, wh = q.pin_memory(), k.pin_memory(), w.pin_memory()
+    idx_h = torch.empty(idx.shape, dtype=torch.int32).pin_memory()
+    sc_h = torch.empty(sc.shape, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        step()
+        idx_h.copy_(idx, non_blocking=True)
+        sc_h.copy_(sc, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 50))
+    barrier(world)
+    return max_over_ranks(time_steps(e2e_step, e2e_steps, stream), world)
+
+
+def emit(args, wl, world, ms, ms_max, flops, pairs, value, rows_per_s, e2e_ms, h2d, d2h,
+         launches_per_step, clk, status, pk, pk_src, lidx):
+    achieved = flops / (ms * 1e-3) / 1e12
+    peak = pk["bf16_tflops"]
+    traffic = recorded_traffic("score_fwd_kernel<64>/long_fused", SCORE_SRC)
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_of(wl, world),
+        "query_rows_per_s": rows_per_s, "valid_pairs_per_step": pairs * world,
+        "tensor_peak_frac": achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "score_fwd_kernel<64> (fused scoring + top-k)",
+                     "peak_source": f"{pk_src} bf16_tflops (burst)",
+                     "algorithmic": f"{pairs} visible pairs x 2*H*D = {flops:.4e} FLOP per launch"},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "device_status": status,
+    }
+    if not args.no_side:
+        line["other_workloads"] = side_workloads(lidx, pk)
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_oracle_sample(wl, args.cpu_stride)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_fused")
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-stride", type=int, default=4)
+    ap.add_argument("--B", type=int, default=0, help="override the workload's batch (profiling)")
+    ap.add_argument("--S", type=int, default=0, help="override the workload's query length "
+                    "(profiling); Skv follows as S // compress_ratio")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-side", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    wl = workloads.WORKLOADS[args.workload]
+    if args.B:
+        wl = wl.with_(B=args.B)
+    if args.S:
+        wl = wl.with_(S=args.S, Skv=args.S // wl.ratio)
+    if args.impl == "reference":
+        run_reference(args, wl, world, rank)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA device (no CPU fallback)")
+        run_gpu(args, wl, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -118,7 +118,7 @@ int lidx_indexer_fwd(const void* q, const void* k, const float* w, int64_t B, in
                      int64_t Skv, int H, int D, int compress_ratio, int topk, int act,
                      const int32_t* topk_indices_in, float* logits_out, int32_t* indices_out,
                      float* scores_out, void* workspace, size_t workspace_bytes, void* stream) {
-    if (!q || !k || !w || !indices_out || !scores_out) return LIDX_ERR_NULL;
+    if (!q || (!k && Skv > 0) || !w || !indices_out || !scores_out) return LIDX_ERR_NULL;
     int rc = check_dims(B, S, Skv, H, D);
     if (rc) return rc;
     if (compress_ratio < 1 || topk < 1 || topk > (1 << 20) || (act != 0 && act != 1))
@@ -129,6 +129,11 @@ int lidx_indexer_fwd(const void* q, const void* k, const float* w, int64_t B, in
     if (Skv > kTopkCandMax) return LIDX_ERR_UNSUPPORTED;
     const int sms = device_sms(true);
     if (sms <= 0) return LIDX_ERR_NO_DEVICE;
+    if (Skv == 0)  // no keys at all: every row is padding, logits has no entries
+        return pad_launch(B * S * (int64_t)topk, indices_out, scores_out, (cudaStream_t)stream) ==
+                       cudaSuccess
+                   ? LIDX_OK
+                   : LIDX_ERR_CUDA;
     ScoreLaunch a;
     memset(&a, 0, sizeof a);
     a.p.B = (int)B;
@@ -160,10 +165,11 @@ int lidx_indexer_fwd(const void* q, const void* k, const float* w, int64_t B, in
 int lidx_indexer_logits(const void* q, const void* k, const float* w, int64_t B, int64_t S,
                         int64_t Skv, int H, int D, int compress_ratio, const int32_t* ks,
                         const int32_t* ke, int clean, int act, float* logits_out, void* stream) {
-    if (!q || !k || !w || !logits_out) return LIDX_ERR_NULL;
+    if (!q || !w || (Skv > 0 && (!k || !logits_out))) return LIDX_ERR_NULL;
     if ((ks == nullptr) != (ke == nullptr)) return LIDX_ERR_NULL;
     int rc = check_dims(B, S, Skv, H, D);
     if (rc) return rc;
+    if (Skv == 0) return LIDX_OK;  // empty output
     if ((!ks && compress_ratio < 1) || (act != 0 && act != 1)) return LIDX_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(w) || !aligned16(logits_out))
         return LIDX_ERR_ALIGN;

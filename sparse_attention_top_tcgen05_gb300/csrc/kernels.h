@@ -45,6 +45,8 @@ size_t score_scratch_bytes(int64_t S, int64_t Skv, int H, int num_sms);
 cudaError_t extract_launch(const float* logits, const int32_t* idx, int64_t rows, int64_t Skv,
                            int topk, float* out, cudaStream_t stream);
 
+cudaError_t pad_launch(int64_t n, int32_t* idx, float* sc, cudaStream_t stream);
+
 // per-TU status readers (see LIDX_STATUS_READER): value, or -1 on a CUDA error
 int status_score_fwd(int clear);
 int status_misc(int clear);

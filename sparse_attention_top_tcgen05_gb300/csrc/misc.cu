@@ -36,6 +36,24 @@ cudaError_t extract_launch(const float* logits, const int32_t* idx, int64_t rows
     return cudaGetLastError();
 }
 
+// Rows with no visible key: index -1 / score -inf everywhere.
+__global__ void pad_kernel(int64_t n, int32_t* __restrict__ idx, float* __restrict__ sc) {
+    const float ninf = __int_as_float(0xff800000);
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        idx[e] = -1;
+        sc[e] = ninf;
+    }
+}
+
+cudaError_t pad_launch(int64_t n, int32_t* idx, float* sc, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    pad_kernel<<<(unsigned)blocks, 256, 0, stream>>>(n, idx, sc);
+    return cudaGetLastError();
+}
+
 LIDX_STATUS_READER(status_misc)
 
 }  // namespace lidx
