@@ -117,6 +117,20 @@ int lidx_extract_topk_scores(const float* logits, const int32_t* idx,
                              float* scores_out, void* stream);
 
 /*
+ * Per-row top-k of given logits   [P1 forward with topk_indices=None: the
+ * selection step; P2 cu_seqlen_ks/cu_seqlen_ke ranges].
+ *   logits fp32 [rows, Skv] row-major, rows = B*S; row r is query s = r % S.
+ *   ks, ke int32 [S] (device), nullable together: NULL -> causal ranges
+ *   [0, min((s+1)/compress_ratio, Skv)).  Only entries in the row's range are
+ *   candidates.  Output as lidx_indexer_fwd: indices_out int32 / scores_out
+ *   fp32 [rows, topk], sorted by score descending, ties by ascending index,
+ *   padded with -1 / -inf.  Limit of this build: visible keys per row <= 4096.
+ */
+int lidx_topk_rows(const float* logits, int64_t rows, int64_t S, int64_t Skv,
+                   int compress_ratio, const int32_t* ks, const int32_t* ke, int topk,
+                   int32_t* indices_out, float* scores_out, void* stream);
+
+/*
  * V4.1 scores   [P3 indexer_scores, module docstring].
  *   q bf16 [B,S,H,D]  k bf16 [B,Skv,D]  w bf16 [B,S,H]  allowed u8/bool [B,S,Skv]
  *   scores_out bf16 [B,S,Skv]: where allowed[b,s,t] != 0,

@@ -10,6 +10,7 @@ Functions carry the C names:
   lidx_indexer_fwd          V4 forward: causal mask + per-row top-k
   lidx_indexer_logits       V4 logits only, causal or explicit [ks, ke) ranges
   lidx_extract_topk_scores  gather of logits at indices
+  lidx_topk_rows            per-row top-k of given logits
   lidx_indexer_scores_v41   V4.1 bf16-rounded scores under a visibility mask
   lidx_indexer_bwd          backward through the selected entries
   lidx_workspace_bytes, lidx_device_status, lidx_status_string
@@ -34,7 +35,7 @@ OP_INDEXER_FWD, OP_INDEXER_BWD, OP_SCORES_V41 = 0, 1, 2
 ACT = {"relu": 0, "identity": 1}
 
 # every symbol include/lidx.h declares
-EXPORTS = ("lidx_indexer_fwd", "lidx_indexer_logits", "lidx_extract_topk_scores",
+EXPORTS = ("lidx_indexer_fwd", "lidx_indexer_logits", "lidx_extract_topk_scores", "lidx_topk_rows",
            "lidx_indexer_scores_v41", "lidx_indexer_bwd", "lidx_workspace_bytes",
            "lidx_device_status", "lidx_status_string", "lidx_version")
 
@@ -66,6 +67,7 @@ def lib() -> C.CDLL:
             L.lidx_indexer_logits.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, P, P, i32,
                                               i32, P, P]
             L.lidx_extract_topk_scores.argtypes = [P, P, i64, i64, i64, i32, P, P]
+            L.lidx_topk_rows.argtypes = [P, i64, i64, i64, i32, P, P, i32, P, P, P]
             L.lidx_indexer_scores_v41.argtypes = [P, P, P, P, i64, i64, i64, i32, i32, i32, P,
                                                   P, sz, P]
             L.lidx_indexer_bwd.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, i32, i32, i32,
@@ -76,7 +78,7 @@ def lib() -> C.CDLL:
             L.lidx_status_string.argtypes = [i32]
             L.lidx_status_string.restype = C.c_char_p
             L.lidx_version.restype = i32
-            for name in ("lidx_indexer_fwd", "lidx_indexer_logits", "lidx_extract_topk_scores",
+            for name in ("lidx_indexer_fwd", "lidx_indexer_logits", "lidx_extract_topk_scores", "lidx_topk_rows",
                          "lidx_indexer_scores_v41", "lidx_indexer_bwd", "lidx_device_status"):
                 getattr(L, name).restype = i32
             _lib = L
@@ -185,6 +187,34 @@ def lidx_extract_topk_scores(logits, idx, stream=None):
                                         _stream(stream))
     _check(rc, "lidx_extract_topk_scores")
     return out
+
+
+def lidx_topk_rows(logits, topk, compress_ratio=1, ks=None, ke=None, stream=None, out=None):
+    """Top-k of each row of logits [B,S,Skv] (or [rows, Skv] with S = rows).
+
+    Visible range per query s: causal from compress_ratio, or [ks[s], ke[s]).
+    Returns (indices [..., topk] int32, scores [..., topk] fp32).
+    """
+    if logits.dim() == 3:
+        B, S, Skv = logits.shape
+    else:
+        _need(logits, "logits", torch.float32, 2)
+        B, (S, Skv) = 1, logits.shape
+    if logits.dtype != torch.float32 or not logits.is_cuda or not logits.is_contiguous():
+        raise ValueError("logits must be a contiguous CUDA float32 tensor")
+    if ks is not None:
+        _need(ks, "ks", torch.int32, 1)
+        _need(ke, "ke", torch.int32, 1)
+    shape = tuple(logits.shape[:-1]) + (topk,)
+    if out is None:
+        idx = torch.empty(shape, dtype=torch.int32, device=logits.device)
+        sc = torch.empty(shape, dtype=torch.float32, device=logits.device)
+    else:
+        idx, sc = out
+    rc = lib().lidx_topk_rows(_ptr(logits), B * S, S, Skv, compress_ratio, _ptr(ks), _ptr(ke), topk,
+                              _ptr(idx), _ptr(sc), _stream(stream))
+    _check(rc, "lidx_topk_rows")
+    return idx, sc
 
 
 def lidx_indexer_scores_v41(q, k, w, allowed, act="relu", stream=None, out=None, workspace=None):

@@ -207,6 +207,27 @@ int lidx_extract_topk_scores(const float* logits, const int32_t* idx, int64_t B,
                : LIDX_ERR_CUDA;
 }
 
+int lidx_topk_rows(const float* logits, int64_t rows, int64_t S, int64_t Skv, int compress_ratio,
+                   const int32_t* ks, const int32_t* ke, int topk, int32_t* indices_out,
+                   float* scores_out, void* stream) {
+    if ((!logits && rows * Skv > 0) || !indices_out || !scores_out) return LIDX_ERR_NULL;
+    if ((ks == nullptr) != (ke == nullptr)) return LIDX_ERR_NULL;
+    if (rows < 0 || S < 1 || Skv < 0 || topk < 1 || topk > (1 << 20) || (!ks && compress_ratio < 1) ||
+        S > (1 << 30) || Skv > (1 << 30))
+        return LIDX_ERR_SHAPE;
+    if (Skv > kTopkCandMax) return LIDX_ERR_UNSUPPORTED;
+    if (device_sms(true) <= 0) return LIDX_ERR_NO_DEVICE;
+    if (Skv == 0)
+        return pad_launch(rows * (int64_t)topk, indices_out, scores_out, (cudaStream_t)stream) ==
+                       cudaSuccess
+                   ? LIDX_OK
+                   : LIDX_ERR_CUDA;
+    return topk_rows_launch(logits, rows, (int)S, (int)Skv, compress_ratio < 1 ? 1 : compress_ratio,
+                            ks, ke, topk, indices_out, scores_out, (cudaStream_t)stream) == cudaSuccess
+               ? LIDX_OK
+               : LIDX_ERR_CUDA;
+}
+
 int lidx_indexer_scores_v41(const void* q, const void* k, const void* w, const uint8_t* allowed,
                             int64_t B, int64_t S, int64_t Skv, int H, int D, int act,
                             void* scores_out, void* workspace, size_t workspace_bytes,

@@ -45,6 +45,9 @@ size_t score_scratch_bytes(int64_t S, int64_t Skv, int H, int num_sms);
 cudaError_t extract_launch(const float* logits, const int32_t* idx, int64_t rows, int64_t Skv,
                            int topk, float* out, cudaStream_t stream);
 
+cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, int ratio,
+                             const int32_t* ks, const int32_t* ke, int topk, int32_t* out_idx,
+                             float* out_sc, cudaStream_t stream);
 cudaError_t pad_launch(int64_t n, int32_t* idx, float* sc, cudaStream_t stream);
 
 // per-TU status readers (see LIDX_STATUS_READER): value, or -1 on a CUDA error

@@ -5,6 +5,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace lidx {
 
@@ -51,6 +52,52 @@ cudaError_t pad_launch(int64_t n, int32_t* idx, float* sc, cudaStream_t stream) 
     int64_t blocks = (n + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     pad_kernel<<<(unsigned)blocks, 256, 0, stream>>>(n, idx, sc);
+    return cudaGetLastError();
+}
+
+// Standalone selection: each CTA (kTopkRowThreads threads) takes rows in turn.
+constexpr int kTopkRowThreads = 256;
+
+__global__ void __launch_bounds__(kTopkRowThreads)
+    topk_rows_kernel(const float* __restrict__ logits, int64_t rows, int S, int Skv, int ratio,
+                     const int32_t* __restrict__ ks, const int32_t* __restrict__ ke, int topk,
+                     int32_t* __restrict__ out_idx, float* __restrict__ out_sc) {
+    extern __shared__ uint8_t smem_raw[];
+    TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        const int s = (int)(r % S);
+        int lo, hi;
+        if (ks == nullptr) {
+            lo = 0;
+            const long long e = (long long)(s + 1) / ratio;
+            hi = (int)(e < Skv ? e : Skv);
+        } else {
+            lo = ks[s] > 0 ? ks[s] : 0;
+            hi = ke[s] < Skv ? ke[s] : Skv;
+            if (hi < lo) hi = lo;
+        }
+        row_topk<kTopkRowThreads>(logits + r * (int64_t)Skv, lo, hi, topk, out_idx + r * topk,
+                                  out_sc + r * topk, sm, threadIdx.x, 1);
+    }
+}
+
+cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, int ratio,
+                             const int32_t* ks, const int32_t* ke, int topk, int32_t* out_idx,
+                             float* out_sc, cudaStream_t stream) {
+    if (rows == 0) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int smem = (int)sizeof(TopkSmem);
+    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_rows_kernel, kTopkRowThreads, smem);
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)sms * per_sm;
+    if (grid > rows) grid = rows;
+    topk_rows_kernel<<<(unsigned)grid, kTopkRowThreads, smem, stream>>>(logits, rows, S, Skv, ratio, ks,
+                                                                        ke, topk, out_idx, out_sc);
     return cudaGetLastError();
 }
 

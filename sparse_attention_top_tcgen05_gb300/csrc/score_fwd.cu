@@ -15,12 +15,15 @@
 //     for the whole key sweep; key tiles [128, D] stream through a 3-stage ring.
 //   * warp 1 lane 0: tcgen05.mma issuer into two 256-column fp32 accumulators
 //     (512 TMEM columns), so the MMA of tile i+1 overlaps the epilogue of tile i.
-//   * warps 2..9: epilogue.  tcgen05.ld -> act -> weighted head sum in fp32 ->
-//     mask -> store (logits) or stash in a per-CTA L2-resident row buffer.
-//     After the query tile's sweep the same 256 threads run the top-k of its
-//     rows (topk.cuh).
+//   * warps 2..5: epilogue, one warp per TMEM lane quadrant.  tcgen05.ld ->
+//     act -> weighted head sum in fp32 (packed f32x2 FMAs) -> mask -> store
+//     (logits) or stash in one of two per-CTA L2-resident row buffers.
+//   * warps 6..13: top-k of the previous query tile's rows (topk.cuh), reading
+//     the row buffer the epilogue is not writing, so selection overlaps the
+//     next tile's key sweep.
 //   * Key tiles past the tile's last visible key are never loaded or multiplied.
-//     Query tiles are dealt to CTAs heaviest-first in a snake order.
+//     Query tiles are dealt to CTAs heaviest-first in a snake order; the next
+//     tile's queries are prefetched into L2 while the current one is swept.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -34,10 +37,13 @@ namespace lidx {
 constexpr int kN = 256;            // UMMA N: query x head columns per tile
 constexpr int kM = 128;            // UMMA M: keys per tile
 constexpr int kStages = 3;         // key-tile ring depth
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+constexpr int kEpiWarps = 4;
+constexpr int kTopkWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
+constexpr int kTopkThreads = 32 * kTopkWarps;
+constexpr int kThreads = 64 + kEpiThreads + kTopkThreads;
 constexpr int kEpiBar = 1;         // named barrier id of the epilogue group
+constexpr int kTopkBar = 2;        // named barrier id of the top-k group
 
 struct Unit {
     int b, s0;
@@ -120,11 +126,44 @@ __host__ __device__ inline SmemLayout smem_layout(int D) {
     L.topk_off = o;
     o += (uint32_t)((sizeof(TopkSmem) + 15) / 16 * 16);
     L.bar_off = o;
-    o += 16 * 8;
+    o += 24 * 8;
     L.tmem_off = o;
     o += 16;
     L.total = o + 1024;  // slack for 1024-byte alignment of the base
     return L;
+}
+
+// Weighted head reduction of one query's H accumulator columns held in
+// registers r[c0 .. c0+H) (c0 compile time): sum_h w[h] * act(x[h]).
+template <int H, int C0, int NR>
+__device__ __forceinline__ float head_sum(const uint32_t (&r)[NR], const float* w, int act) {
+    if constexpr (H >= 4) {
+        const float4* w4 = reinterpret_cast<const float4*>(w);
+        uint64_t a0 = 0, a1 = 0;  // two packed accumulators = four independent chains
+#pragma unroll
+        for (int h = 0; h < H; h += 4) {
+            const float4 wv = w4[h / 4];
+            float x0 = __uint_as_float(r[C0 + h]), x1 = __uint_as_float(r[C0 + h + 1]);
+            float x2 = __uint_as_float(r[C0 + h + 2]), x3 = __uint_as_float(r[C0 + h + 3]);
+            if (act == 0) {
+                x0 = fmaxf(x0, 0.f);
+                x1 = fmaxf(x1, 0.f);
+                x2 = fmaxf(x2, 0.f);
+                x3 = fmaxf(x3, 0.f);
+            }
+            a0 = fma2(pack2(x0, x1), pack2(wv.x, wv.y), a0);
+            a1 = fma2(pack2(x2, x3), pack2(wv.z, wv.w), a1);
+        }
+        float p0, p1, p2, p3;
+        unpack2(a0, p0, p1);
+        unpack2(a1, p2, p3);
+        return (p0 + p1) + (p2 + p3);
+    } else {
+        float acc = 0.f;
+#pragma unroll
+        for (int h = 0; h < H; ++h) acc = fmaf(w[h], act_f(__uint_as_float(r[C0 + h]), act), acc);
+        return acc;
+    }
 }
 
 template <int H>
@@ -144,14 +183,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = (uint64_t*)(smem + L.bar_off);
     uint64_t* q_full = bars + 0;
     uint64_t* q_empty = bars + 1;
-    uint64_t* k_full = bars + 2;              // [kStages]
-    uint64_t* k_empty = bars + 2 + kStages;   // [kStages]
+    uint64_t* k_full = bars + 2;                  // [kStages]
+    uint64_t* k_empty = bars + 2 + kStages;       // [kStages]
     uint64_t* acc_full = bars + 2 + 2 * kStages;  // [2]
     uint64_t* acc_empty = acc_full + 2;           // [2]
+    uint64_t* rows_full = acc_empty + 2;          // [2] epilogue -> top-k
+    uint64_t* rows_empty = rows_full + 2;         // [2] top-k -> epilogue
     uint32_t* tmem_slot = (uint32_t*)(smem + L.tmem_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int swz = p.swz, KB = swz / 2, nkb = p.D / KB;
+    const bool materialise = p.logits != nullptr;
+    const bool select = p.topk > 0;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -163,6 +206,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full + i, 1);
             mbar_init(acc_empty + i, kEpiWarps);
+            mbar_init(rows_full + i, kEpiThreads);
+            mbar_init(rows_empty + i, kTopkThreads);
         }
         fence_mbar_init();
         tma_prefetch_desc(&tmq);
@@ -193,6 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive_expect_tx(q_full, kN * p.D * 2);
                 for (int kb = 0; kb < nkb; ++kb)
                     tma_load_4d(sQ + kb * kN * swz, &tmq, q_full, kb * KB, 0, un.b, un.s0);
+                // warm L2 with the next query tile of this CTA
+                const int un2 = unit_of(i + 1, p.num_units);
+                if (un2 >= 0) {
+                    const int qt2 = p.qtiles - 1 - un2 / p.B;
+                    for (int kb = 0; kb < nkb; ++kb)
+                        tma_prefetch_l2_4d(&tmq, kb * KB, 0, un2 % p.B, qt2 * QT);
+                }
                 for (int kt = un.lo_t; kt < un.hi_t; ++kt, ++kcount) {
                     const int st = kcount % kStages;
                     if (!(ok = mbar_wait(k_empty + st, ((kcount / kStages) & 1) ^ 1))) break;
@@ -239,25 +291,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) umma_commit(q_empty);
             }
         }
-    } else {
+    } else if (warp < 2 + kEpiWarps) {
         // --------------------------------------------------------- epilogue
         const int etid = threadIdx.x - 64;
         const int quad = warp & 3;           // TMEM lane quadrant this warp may read
-        const int half = (warp - 2) >> 2;    // which 128 of the 256 columns
         const int row_t = quad * 32 + lane;  // key within the tile
-        constexpr int QH = QT / 2;           // queries per half (H <= 128)
         const float ninf = __int_as_float(0xff800000);
         const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
         const int ntiles_all = (p.Skv + kM - 1) / kM;
-        const bool materialise = p.logits != nullptr;
-        int tcount = 0;
+        int tcount = 0, ucount = 0;
         bool ok = true;
-        float* scratch = p.scratch ? p.scratch + (size_t)blockIdx.x * p.scratch_stride_cta : nullptr;
         for (int i = 0; ok; ++i) {
             const int u = unit_of(i, p.num_units);
             if (u == -2) break;
             if (u < 0) continue;
             const Unit un = make_unit<QT>(p, u);
+            const int rb = ucount & 1;
+            float* rows = nullptr;
+            if (select) {
+                // the top-k group must have finished the tile that last used slot rb
+                // (this also keeps the row barriers at most one phase apart)
+                if (!(ok = mbar_wait(rows_empty + rb, ((ucount >> 1) & 1) ^ 1))) break;
+                if (!materialise)
+                    rows = p.scratch + ((size_t)blockIdx.x * 2 + rb) * p.scratch_stride_cta;
+            }
             named_bar_sync(kEpiBar, kEpiThreads);
             for (int e = etid; e < kN; e += kEpiThreads) {
                 const int ql = e / H, h = e % H, s = un.s0 + ql;
@@ -273,72 +330,102 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(kEpiBar, kEpiThreads);
             const int t_begin = materialise ? 0 : un.lo_t;
             const int t_end = materialise ? ntiles_all : un.hi_t;
-            const float* wh = sW + half * 128;
             for (int kt = t_begin; kt < t_end; ++kt) {
                 const int t = kt * kM + row_t;
                 const bool computed = kt >= un.lo_t && kt < un.hi_t;
                 if (!computed) {
                     // tile outside every row's range: masked fill only
                     if (p.clean && t < p.Skv)
-                        for (int j = 0; j < QH; ++j) {
-                            const int ql = half * QH + j;
+                        for (int ql = 0; ql < QT; ++ql)
                             if (sHi[ql] >= 0)
                                 p.logits[((size_t)un.b * p.S + un.s0 + ql) * p.Skv + t] = ninf;
-                        }
                     continue;
                 }
                 const int acc = tcount & 1;
                 if (!(ok = mbar_wait(acc_full + acc, (tcount >> 1) & 1))) break;
                 ++tcount;
                 tc_fence_after();
-                // this half's 128 accumulator columns, as 4 chunks of 32
-                uint32_t r[4][32];
+                auto store = [&](int ql, float v) {
+                    const int lo = sLo[ql], hi = sHi[ql];
+                    if (hi < 0) return;
+                    const bool vis = t >= lo && t < hi;
+                    if (materialise) {
+                        if (t < p.Skv && (vis || p.clean))
+                            p.logits[((size_t)un.b * p.S + un.s0 + ql) * p.Skv + t] = vis ? v : ninf;
+                    } else if (rows) {
+                        rows[(size_t)ql * p.Skv_pad + t] = v;
+                    }
+                };
+                float carry = 0.f;  // partial sum of a query spanning two column groups (H = 128)
 #pragma unroll
-                for (int c = 0; c < 4; ++c) tmem_ld32(lane_addr + acc * kN + (half * 4 + c) * 32, r[c]);
-                tmem_ld_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty + acc);  // accumulator may be reused
-                float run = 0.f;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-#pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int cih = c * 32 + jj;  // column within the half (compile time)
-                        const int j = cih / H, h = cih % H;
-                        const float x = __uint_as_float(r[c][jj]);
-                        run = fmaf(wh[cih], act_f(x, p.act), h == 0 ? 0.f : run);
-                        if (h == H - 1) {
-                            const int ql = half * QH + j;
-                            const int lo = sLo[ql], hi = sHi[ql];
-                            if (hi >= 0) {
-                                const bool vis = t >= lo && t < hi;
-                                if (materialise) {
-                                    if (t < p.Skv && (vis || p.clean))
-                                        p.logits[((size_t)un.b * p.S + un.s0 + ql) * p.Skv + t] =
-                                            vis ? run : ninf;
-                                } else {
-                                    scratch[(size_t)ql * p.Skv_pad + t] = run;
-                                }
-                            }
+                for (int pr = 0; pr < 4; ++pr) {
+                    // columns [64*pr, 64*pr + 64) of the accumulator
+                    uint32_t r[64];
+                    tmem_ld32(lane_addr + acc * kN + pr * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                    tmem_ld32(lane_addr + acc * kN + pr * 64 + 32,
+                              *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    tmem_ld_wait();
+                    if (pr == 3) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(acc_empty + acc);  // accumulator may be reused
+                    }
+                    const float* wp = sW + pr * 64;
+                    if constexpr (H == 128) {
+                        carry += head_sum<64, 0>(r, wp, p.act);
+                        if (pr & 1) {
+                            store(pr >> 1, carry);
+                            carry = 0.f;
                         }
+                    } else if constexpr (H == 64) {
+                        store(pr, head_sum<64, 0>(r, wp, p.act));
+                    } else if constexpr (H == 32) {
+                        store(pr * 2, head_sum<32, 0>(r, wp, p.act));
+                        store(pr * 2 + 1, head_sum<32, 32>(r, wp + 32, p.act));
+                    } else {
+#pragma unroll
+                        for (int qq = 0; qq < 64 / H; ++qq)
+                            store(pr * (64 / H) + qq,
+                                  head_sum<H, 0>(*reinterpret_cast<const uint32_t(*)[64]>(&r[qq * H]),
+                                                 wp + qq * H, p.act));
                     }
                 }
             }
             if (!ok) break;
-            if (p.topk > 0) {
-                named_bar_sync(kEpiBar, kEpiThreads);  // row buffers complete and visible
-                for (int ql = 0; ql < QT; ++ql) {
-                    const int s = un.s0 + ql;
-                    if (s >= p.S) break;
-                    const int lo = sLo[ql], hi = sHi[ql];
-                    const size_t orow = ((size_t)un.b * p.S + s) * p.topk;
-                    const float* row = materialise ? p.logits + ((size_t)un.b * p.S + s) * p.Skv
-                                                   : scratch + (size_t)ql * p.Skv_pad;
-                    row_topk<kEpiThreads>(row, lo, hi, p.topk, p.out_idx + orow, p.out_sc + orow, sT,
-                                          etid, kEpiBar);
-                }
+            if (select) {
+                // publish this tile's rows to the top-k group (release on arrive)
+                mbar_arrive(rows_full + rb);
             }
+            ++ucount;
+        }
+    } else {
+        // ------------------------------------------------------------ top-k
+        const int ttid = threadIdx.x - 64 - kEpiThreads;
+        int ucount = 0;
+        bool ok = true;
+        for (int i = 0; ok && select; ++i) {
+            const int u = unit_of(i, p.num_units);
+            if (u == -2) break;
+            if (u < 0) continue;
+            const Unit un = make_unit<QT>(p, u);
+            const int rb = ucount & 1;
+            if (!(ok = mbar_wait(rows_full + rb, (ucount >> 1) & 1))) break;
+            const float* rows = materialise
+                                    ? nullptr
+                                    : p.scratch + ((size_t)blockIdx.x * 2 + rb) * p.scratch_stride_cta;
+            for (int ql = 0; ql < QT; ++ql) {
+                const int s = un.s0 + ql;
+                if (s >= p.S) break;
+                int lo, hi;
+                row_range(p, s, lo, hi);
+                const size_t orow = ((size_t)un.b * p.S + s) * p.topk;
+                const float* row = materialise ? p.logits + ((size_t)un.b * p.S + s) * p.Skv
+                                               : rows + (size_t)ql * p.Skv_pad;
+                row_topk<kTopkThreads>(row, lo, hi, p.topk, p.out_idx + orow, p.out_sc + orow, sT,
+                                       ttid, kTopkBar);
+            }
+            mbar_arrive(rows_empty + rb);
+            ++ucount;
         }
     }
 
@@ -391,7 +478,7 @@ size_t score_scratch_bytes(int64_t S, int64_t Skv, int H, int num_sms) {
     (void)S;
     const int QT = kN / H;
     const int64_t Skv_pad = (Skv + kM - 1) / kM * kM;
-    return (size_t)num_sms * QT * Skv_pad * sizeof(float);
+    return (size_t)num_sms * 2 * QT * Skv_pad * sizeof(float);  // two row buffers per CTA
 }
 
 int score_fwd_launch(ScoreLaunch& a) {

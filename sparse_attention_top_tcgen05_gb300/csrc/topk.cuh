@@ -8,7 +8,8 @@
 // index -1 / score -inf.
 //
 // Method (value-linear bucketing, exact):
-//   1. min and max of the row's visible scores.
+//   1. the row's visible scores are staged in shared memory (many loads in
+//      flight per thread), taking their min and max on the way.
 //   2. NB buckets linear in (max - v): bucket(v) = floor((max - v) * NB/(max-min)),
 //      clamped.  IEEE subtraction and multiplication are monotone, so a lower
 //      bucket always holds strictly larger scores than a higher one.
@@ -18,7 +19,7 @@
 //      bucket, into shared memory.
 //   5. Each member's final position is its bucket's start plus its rank among
 //      the bucket's members under (score desc, index asc); positions < topk
-//      are written.  Buckets are small for continuous scores; many exactly
+//      are recorded in shared memory and written out coalesced.  Buckets are small for continuous scores; many exactly
 //      equal scores make a bucket large and that step quadratic in its size.
 #pragma once
 #include <stdint.h>
@@ -31,10 +32,10 @@ constexpr int kTopkBuckets = 2048;
 constexpr int kTopkCandMax = 4096;  // visible keys per row the selection supports
 
 struct TopkSmem {
-    int start[kTopkBuckets + 1];
-    int cursor[kTopkBuckets];
-    float cand_v[kTopkCandMax];
-    int cand_i[kTopkCandMax];
+    float row[kTopkCandMax];          // the row's visible scores, staged once
+    int start[kTopkBuckets + 1];      // bucket offsets; after the scatter, bucket ends
+    uint16_t cand[kTopkCandMax];      // candidate keys (offsets into row), grouped by bucket
+    uint16_t perm[kTopkCandMax];      // key at each output position
     float red_max[32];
     float red_min[32];
     int wsum[32];
@@ -47,25 +48,39 @@ __device__ __forceinline__ int topk_bucket(float v, float vmax, float scale) {
     return b < kTopkBuckets ? b : kTopkBuckets - 1;
 }
 
-// Selects the top `topk` of row[lo..hi) (row is global, L2-resident).
-// All NT threads of the group must call it with identical scalar arguments.
+// Selects the top `topk` of row[lo..hi) (row is global, L2-resident) into
+// out_idx/out_sc.  All NT threads of the group must call it with identical
+// scalar arguments; hi - lo must not exceed kTopkCandMax.
 template <int NT>
 __device__ void row_topk(const float* row, int lo, int hi, int topk, int32_t* out_idx,
                          float* out_sc, TopkSmem& sm, int tid, int bar_id) {
     static_assert(NT % 32 == 0 && NT <= 1024, "group size");
     constexpr int NW = NT / 32;
+    constexpr int UNR = 8;  // loads in flight per thread while staging
     const int lane = tid & 31, wid = tid >> 5;
     const int n = hi > lo ? hi - lo : 0;
     const int sel = n < topk ? n : topk;
     const float ninf = __int_as_float(0xff800000);
 
     if (n > 0) {
-        // 1. min / max
+        // 1. stage the row in shared memory; min / max on the way
         float vmax = ninf, vmin = __int_as_float(0x7f800000);
-        for (int t = lo + tid; t < hi; t += NT) {
-            float v = row[t];
-            vmax = fmaxf(vmax, v);
-            vmin = fminf(vmin, v);
+        for (int base = 0; base < n; base += NT * UNR) {
+            float v[UNR];
+#pragma unroll
+            for (int k = 0; k < UNR; ++k) {
+                const int j = base + k * NT + tid;
+                v[k] = j < n ? row[lo + j] : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < UNR; ++k) {
+                const int j = base + k * NT + tid;
+                if (j < n) {
+                    sm.row[j] = v[k];
+                    vmax = fmaxf(vmax, v[k]);
+                    vmin = fminf(vmin, v[k]);
+                }
+            }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
@@ -76,6 +91,7 @@ __device__ void row_topk(const float* row, int lo, int hi, int topk, int32_t* ou
             sm.red_max[wid] = vmax;
             sm.red_min[wid] = vmin;
         }
+        for (int i = tid; i <= kTopkBuckets; i += NT) sm.start[i] = 0;
         named_bar_sync(bar_id, NT);
         vmax = sm.red_max[0];
         vmin = sm.red_min[0];
@@ -87,79 +103,76 @@ __device__ void row_topk(const float* row, int lo, int hi, int topk, int32_t* ou
 
         if (!(vmax > vmin)) {
             // every visible score is equal: the first `sel` keys in index order
-            for (int j = tid; j < sel; j += NT) {
-                out_idx[j] = lo + j;
-                out_sc[j] = row[lo + j];
-            }
+            for (int j = tid; j < sel; j += NT) sm.perm[j] = (uint16_t)j;
         } else {
             float scale = (float)kTopkBuckets / __fsub_rn(vmax, vmin);
             if (!(scale < __int_as_float(0x7f800000))) scale = 0.f;  // overflowed range
             // 2. histogram
-            for (int i = tid; i <= kTopkBuckets; i += NT) sm.start[i] = 0;
+#pragma unroll 4
+            for (int j = tid; j < n; j += NT) atomicAdd(&sm.start[topk_bucket(sm.row[j], vmax, scale)], 1);
             named_bar_sync(bar_id, NT);
-            for (int t = lo + tid; t < hi; t += NT) atomicAdd(&sm.start[topk_bucket(row[t], vmax, scale)], 1);
+            // 3. exclusive scan.  Warp w owns buckets [w*SEG, (w+1)*SEG); lane l
+            //    reads buckets l, l+32, ... of it, so reads hit 32 distinct banks.
+            constexpr int SEG = kTopkBuckets / NW;
+            static_assert(kTopkBuckets % (NW * 32) == 0, "bucket split");
+            {
+                int wtotal = 0;
+#pragma unroll 4
+                for (int i = 0; i < SEG; i += 32) wtotal += sm.start[wid * SEG + i + lane];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) wtotal += __shfl_xor_sync(0xffffffffu, wtotal, o);
+                if (lane == 0) sm.wsum[wid] = wtotal;
+            }
             named_bar_sync(bar_id, NT);
-            // 3. exclusive scan; each thread owns a run of consecutive buckets
-            constexpr int PER = kTopkBuckets / NT;
-            static_assert(kTopkBuckets % NT == 0, "bucket split");
-            int cnt[PER];
-            int local = 0;
+            int carry = 0;
+            for (int i = 0; i < wid; ++i) carry += sm.wsum[i];
+            for (int i = 0; i < SEG; i += 32) {
+                const int b = wid * SEG + i + lane;
+                const int c = sm.start[b];
+                int incl = c;
 #pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                cnt[i] = sm.start[tid * PER + i];
-                local += cnt[i];
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int excl = carry + incl - c;
+                sm.start[b] = excl;
+                if (excl < sel && excl + c >= sel) sm.bstar = b;
+                carry += __shfl_sync(0xffffffffu, incl, 31);
             }
-            int incl = local;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                int y = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (lane == 31) sm.wsum[wid] = incl;
-            named_bar_sync(bar_id, NT);
-            int base = incl - local;
-            for (int i = 0; i < wid; ++i) base += sm.wsum[i];
-#pragma unroll
-            for (int i = 0; i < PER; ++i) {
-                const int b = tid * PER + i;
-                sm.start[b] = base;
-                sm.cursor[b] = base;
-                if (base < sel && base + cnt[i] >= sel) sm.bstar = b;
-                base += cnt[i];
-            }
-            if (tid == NT - 1) sm.start[kTopkBuckets] = base;  // == n
             named_bar_sync(bar_id, NT);
             const int bstar = sm.bstar;
-            const int ncand = sm.start[bstar + 1];
-            // 4. scatter the candidates, grouped by bucket
-            for (int t = lo + tid; t < hi; t += NT) {
-                float v = row[t];
-                int b = topk_bucket(v, vmax, scale);
-                if (b <= bstar) {
-                    int slot = atomicAdd(&sm.cursor[b], 1);
-                    sm.cand_v[slot] = v;
-                    sm.cand_i[slot] = t;
-                }
+            // 4. scatter the candidates, grouped by bucket; start[b] becomes
+            //    the end of bucket b (== start of b+1) for every b <= bstar
+#pragma unroll 4
+            for (int j = tid; j < n; j += NT) {
+                const int b = topk_bucket(sm.row[j], vmax, scale);
+                if (b <= bstar) sm.cand[atomicAdd(&sm.start[b], 1)] = (uint16_t)j;
             }
             named_bar_sync(bar_id, NT);
-            // 5. rank inside the bucket
-            for (int p = tid; p < ncand; p += NT) {
-                float v = sm.cand_v[p];
-                int t = sm.cand_i[p];
-                int b = topk_bucket(v, vmax, scale);
-                int s0 = sm.start[b], e0 = sm.start[b + 1];
+            const int ncand = sm.start[bstar];
+            // 5. rank inside the bucket [end(b-1), end(b)); record the key at its position
+            for (int pidx = tid; pidx < ncand; pidx += NT) {
+                const int j = sm.cand[pidx];
+                const float v = sm.row[j];
+                const int b = topk_bucket(v, vmax, scale);
+                const int s0 = b == 0 ? 0 : sm.start[b - 1], e0 = sm.start[b];
                 int rank = 0;
                 for (int qq = s0; qq < e0; ++qq) {
-                    float vq = sm.cand_v[qq];
-                    int iq = sm.cand_i[qq];
-                    rank += (vq > v) || (vq == v && iq < t);
+                    const int jq = sm.cand[qq];
+                    const float vq = sm.row[jq];
+                    rank += (vq > v) || (vq == v && jq < j);
                 }
-                int pos = s0 + rank;
-                if (pos < sel) {
-                    out_idx[pos] = t;
-                    out_sc[pos] = v;
-                }
+                const int pos = s0 + rank;
+                if (pos < sel) sm.perm[pos] = (uint16_t)j;
             }
+        }
+        named_bar_sync(bar_id, NT);
+        // 6. coalesced output
+        for (int p = tid; p < sel; p += NT) {
+            const int j = sm.perm[p];
+            out_idx[p] = lo + j;
+            out_sc[p] = sm.row[j];
         }
     }
     for (int j = sel + tid; j < topk; j += NT) {

@@ -170,6 +170,11 @@ def test_edge_cases():
     k = torch.zeros_like(k)
     idx, sc, _ = run_fwd(q, k, w, 4, 6, False)
     assert (idx[0, -1] == np.arange(6)).all() and (sc[0, -1] == 0).all()
+    # one outlier key and many exact zeros: one bucket holds almost the whole row
+    q, k, w = workloads.integer_inputs(1, 256, 64, 8, 32, seed=11)
+    kk = torch.zeros_like(k)
+    kk[5] = k[5]
+    full_check(q, kk, w, 1, 16)
     # heavy ties from integer inputs: exact comparison on the kernel's logits
     q, k, w = workloads.integer_inputs(2, 400, 100, 8, 32, seed=10)
     full_check(q, k, w, 4, 40)
