@@ -94,6 +94,29 @@ int lidx_indexer_fwd(const void* q, const void* k, const float* w,
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The fused forward of lidx_indexer_fwd (logits not written, selection made)
+ * without a caller-supplied workspace.  The indexer pages have no counterpart:
+ * this call exists for callers that cannot allocate device memory (code that
+ * runs inside an allocator or memory-pool callback, in a process whose device
+ * memory is reserved up front by another framework, or in a plug-in that only
+ * receives input and output pointers).  Its scratch is one array inside the
+ * library of lidx_noalloc_scratch_bytes() bytes (24 MiB), held on every GPU
+ * that loads the library until the process exits.  Arguments and outputs are
+ * those of lidx_indexer_fwd.  Returns LIDX_ERR_WORKSPACE when the call would
+ * need more scratch than the array holds (lidx_workspace_bytes(...) >
+ * lidx_noalloc_scratch_bytes(); e.g. at H=64 about 2*4*Skv*4 bytes per SM).
+ * The first call on a device looks up the array's address; make it before any
+ * stream capture.  Calls share the array: calls that overlap on the GPU race.
+ */
+int lidx_indexer_fwd_noalloc(const void* q, const void* k, const float* w,
+                             int64_t B, int64_t S, int64_t Skv, int H, int D,
+                             int compress_ratio, int topk, int act,
+                             int32_t* indices_out, float* scores_out, void* stream);
+
+/* Size in bytes of the scratch array lidx_indexer_fwd_noalloc uses. */
+size_t lidx_noalloc_scratch_bytes(void);
+
+/*
  * Logits only, explicit ranges   [P2 batched_indexer_fwd, indexer_fwd_interface,
  * clean_logits_].  Same layouts as lidx_indexer_fwd.
  *   ks, ke  int32 [S] (device), nullable together: NULL -> causal ranges from

@@ -37,7 +37,8 @@ ACT = {"relu": 0, "identity": 1}
 # every symbol include/lidx.h declares
 EXPORTS = ("lidx_indexer_fwd", "lidx_indexer_logits", "lidx_extract_topk_scores", "lidx_topk_rows",
            "lidx_indexer_scores_v41", "lidx_indexer_bwd", "lidx_workspace_bytes",
-           "lidx_device_status", "lidx_status_string", "lidx_version")
+           "lidx_device_status", "lidx_status_string", "lidx_version",
+           "lidx_indexer_fwd_noalloc", "lidx_noalloc_scratch_bytes")
 
 
 class LidxError(RuntimeError):
@@ -72,6 +73,10 @@ def lib() -> C.CDLL:
                                                   P, sz, P]
             L.lidx_indexer_bwd.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, i32, i32, i32,
                                            i32, P, P, P, P, sz, P]
+            L.lidx_indexer_fwd_noalloc.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, i32, i32,
+                                                   P, P, P]
+            L.lidx_indexer_fwd_noalloc.restype = i32
+            L.lidx_noalloc_scratch_bytes.restype = sz
             L.lidx_workspace_bytes.argtypes = [i32, i64, i64, i64, i32, i32, i32, i32]
             L.lidx_workspace_bytes.restype = sz
             L.lidx_device_status.argtypes = [P]
@@ -156,6 +161,26 @@ def lidx_indexer_fwd(q, k, w, compress_ratio, topk, act="relu", topk_indices=Non
                                 _stream(stream))
     _check(rc, "lidx_indexer_fwd")
     return idx, sc, lg
+
+
+def lidx_indexer_fwd_noalloc(q, k, w, compress_ratio, topk, act="relu", stream=None, out=None):
+    """The fused V4 forward using the library's own scratch array instead of a
+    workspace, for callers that cannot allocate device memory.  Outputs may be
+    passed in ``out`` = (indices, scores) so that the call allocates nothing."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(w, "w", torch.float32, 3)
+    S, B, H, D = q.shape
+    Skv = k.shape[0]
+    if out is None:
+        idx = torch.empty(B, S, topk, dtype=torch.int32, device=q.device)
+        sc = torch.empty(B, S, topk, dtype=torch.float32, device=q.device)
+    else:
+        idx, sc = out
+    rc = lib().lidx_indexer_fwd_noalloc(_ptr(q), _ptr(k), _ptr(w), B, S, Skv, H, D, compress_ratio,
+                                        topk, ACT[act], _ptr(idx), _ptr(sc), _stream(stream))
+    _check(rc, "lidx_indexer_fwd_noalloc")
+    return idx, sc
 
 
 def lidx_indexer_logits(q, k, w, compress_ratio=1, ks=None, ke=None, clean=True, act="relu",
