@@ -103,6 +103,13 @@ size_t lidx_workspace_bytes(int op, int64_t B, int64_t S, int64_t Skv, int H, in
         if (logits_materialised || topk <= 0 || !pow2_heads(H)) return 0;
         return score_scratch_bytes(S, Skv, H, sms);
     }
+    if (op == LIDX_OP_SCORES_V41) {
+        // one byte per (batch, query tile, 128-key tile): the visibility tile map
+        if (!pow2_heads(H) || Skv <= 0 || B <= 0 || S <= 0) return 0;
+        const int64_t QT = score_query_tile(H);
+        const int64_t bytes = B * ((S + QT - 1) / QT) * ((Skv + 127) / 128);
+        return (size_t)((bytes + 255) / 256 * 256);
+    }
     return 0;
 }
 
@@ -232,14 +239,41 @@ int lidx_indexer_scores_v41(const void* q, const void* k, const void* w, const u
                             int64_t B, int64_t S, int64_t Skv, int H, int D, int act,
                             void* scores_out, void* workspace, size_t workspace_bytes,
                             void* stream) {
-    (void)workspace;
-    (void)workspace_bytes;
-    (void)stream;
-    if (!q || !k || !w || !allowed || !scores_out) return LIDX_ERR_NULL;
+    if (!q || !w || (Skv > 0 && (!k || !allowed || !scores_out))) return LIDX_ERR_NULL;
     int rc = check_dims(B, S, Skv, H, D);
     if (rc) return rc;
-    (void)act;
-    return LIDX_ERR_UNSUPPORTED;
+    if (act != 0 && act != 1) return LIDX_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(w) || ((uintptr_t)scores_out & 1u))
+        return LIDX_ERR_ALIGN;
+    if (Skv == 0) return LIDX_OK;  // empty output
+    const int sms = device_sms(true);
+    if (sms <= 0) return LIDX_ERR_NO_DEVICE;
+    const size_t need = lidx_workspace_bytes(LIDX_OP_SCORES_V41, B, S, Skv, H, D, 0, 0);
+    if (!workspace || workspace_bytes < need) return LIDX_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    // 1. visibility pass: tile map + -inf for blocks with no visible pair
+    if (v41_mask_launch(allowed, (uint16_t*)scores_out, (uint8_t*)workspace, (int)B, (int)S,
+                        (int)Skv, score_query_tile(H), st) != cudaSuccess)
+        return LIDX_ERR_CUDA;
+    // 2. tensor-core pass over the blocks with work
+    ScoreLaunch a;
+    memset(&a, 0, sizeof a);
+    a.p.B = (int)B;
+    a.p.S = (int)S;
+    a.p.Skv = (int)Skv;
+    a.p.H = H;
+    a.p.D = D;
+    a.p.ratio = 1;
+    a.p.act = act;
+    a.p.w16 = (const uint16_t*)w;
+    a.p.allowed = allowed;
+    a.p.out16 = (uint16_t*)scores_out;
+    a.p.tilemap = (const uint8_t*)workspace;
+    a.q = q;
+    a.k = k;
+    a.stream = stream;
+    a.num_sms = sms;
+    return score_v41_launch(a) == 0 ? LIDX_OK : LIDX_ERR_CUDA;
 }
 
 int lidx_indexer_bwd(const void* q, const void* k, const float* w, const int32_t* idx,

@@ -21,6 +21,12 @@ struct ScoreParams {
     int topk;           // 0: no selection
     int32_t* out_idx;   // [B,S,topk]
     float* out_sc;      // [B,S,topk]
+    // V4.1 (BSHD layouts, bf16 weights and scores, explicit visibility)
+    const uint16_t* w16;      // [B,S,H] bf16
+    const uint8_t* allowed;   // [B,S,Skv]
+    uint16_t* out16;          // [B,S,Skv] bf16
+    const uint8_t* tilemap;   // [B, qtiles, ntk]: 1 where the block has a visible pair
+    int ntk;                  // key tiles per row
     // filled by the launcher
     int num_units, qtiles, Skv_pad, swz;
 };
@@ -40,6 +46,10 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* ad
                  const cuuint32_t* elem_strides, CUtensorMapSwizzle swizzle);
 
 int score_fwd_launch(ScoreLaunch& a);
+int score_v41_launch(ScoreLaunch& a);
+int score_query_tile(int H);  // query rows per tile for H heads
+cudaError_t v41_mask_launch(const uint8_t* allowed, uint16_t* out, uint8_t* tilemap, int B, int S,
+                            int Skv, int QT, cudaStream_t stream);
 size_t score_scratch_bytes(int64_t S, int64_t Skv, int H, int num_sms);
 
 cudaError_t extract_launch(const float* logits, const int32_t* idx, int64_t rows, int64_t Skv,

@@ -46,7 +46,7 @@ constexpr int kEpiBar = 1;         // named barrier id of the epilogue group
 constexpr int kTopkBar = 2;        // named barrier id of the top-k group
 
 struct Unit {
-    int b, s0;
+    int b, s0, qt;
     int lo_t, hi_t;  // key tiles [lo_t, hi_t) with work
     int lo_k, hi_k;  // visible keys of the tile's union range
 };
@@ -63,13 +63,29 @@ __device__ __forceinline__ void row_range(const ScoreParams& p, int s, int& lo, 
     }
 }
 
-template <int QT>
+template <int QT, bool V41>
 __device__ __forceinline__ Unit make_unit(const ScoreParams& p, int u) {
     Unit un;
     const int qt = p.qtiles - 1 - u / p.B;  // heaviest (latest) query tiles first
     un.b = u % p.B;
+    un.qt = qt;
     un.s0 = qt * QT;
     const int s_last = min(un.s0 + QT - 1, p.S - 1);
+    if constexpr (V41) {
+        // key tiles with any visible pair come from the visibility tile map
+        const uint8_t* m = p.tilemap + ((size_t)un.b * p.qtiles + qt) * p.ntk;
+        int first = -1, last = -1;
+        for (int kt = 0; kt < p.ntk; ++kt)
+            if (m[kt]) {
+                if (first < 0) first = kt;
+                last = kt;
+            }
+        un.lo_t = first < 0 ? 0 : first;
+        un.hi_t = first < 0 ? 0 : last + 1;
+        un.lo_k = un.lo_t * kM;
+        un.hi_k = min(un.hi_t * kM, p.Skv);
+        return un;
+    }
     if (p.ks == nullptr) {
         int lo, hi;
         row_range(p, s_last, lo, hi);
@@ -95,6 +111,12 @@ __device__ __forceinline__ Unit make_unit(const ScoreParams& p, int u) {
         un.lo_t = un.hi_t = 0;
     }
     return un;
+}
+
+template <bool V41>
+__device__ __forceinline__ bool tile_active(const ScoreParams& p, const Unit& un, int kt) {
+    if constexpr (V41) return p.tilemap[((size_t)un.b * p.qtiles + un.qt) * p.ntk + kt] != 0;
+    return true;
 }
 
 // i-th unit of this CTA in snake order, or -1 when past the end
@@ -166,7 +188,54 @@ __device__ __forceinline__ float head_sum(const uint32_t (&r)[NR], const float* 
     }
 }
 
-template <int H>
+__device__ __forceinline__ uint32_t cvt_bf16x2(float hi, float lo) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ float bf16_round_f(float x) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r << 16);
+}
+
+// V4.1 head reduction of one query ("deepseek_v41.indexer" page, module
+// docstring): y = bf16(x); z = bf16(act(y) * w); fp32 sum of z over heads.
+// wp holds the query's bf16 weights as pairs (low half = even head); for H = 1
+// one weight per word.  The product of two bf16 values is exact, so rounding it
+// once to bf16 is the stated rounding of the weighted head score.
+template <int H, int NR>
+__device__ __forceinline__ float head_sum_v41(const uint32_t (&r)[NR], int c0, const uint32_t* wp,
+                                              int act) {
+    if constexpr (H >= 2) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int h = 0; h < H; h += 2) {
+            uint32_t y2 = cvt_bf16x2(__uint_as_float(r[c0 + h + 1]), __uint_as_float(r[c0 + h]));
+            if (act == 0) y2 = max_bf16x2(y2, 0u);
+            const uint32_t z2 = mul_bf16x2(y2, wp[h / 2]);
+            s0 += __uint_as_float(z2 << 16);
+            s1 += __uint_as_float(z2 & 0xffff0000u);
+        }
+        return s0 + s1;
+    } else {
+        float y = bf16_round_f(__uint_as_float(r[c0]));
+        if (act == 0) y = fmaxf(y, 0.f);
+        return bf16_round_f(y * __uint_as_float(wp[0] << 16));
+    }
+}
+
+template <int H, bool V41>
 __global__ void __launch_bounds__(kThreads, 1)
     score_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const ScoreParams p) {
@@ -193,8 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int swz = p.swz, KB = swz / 2, nkb = p.D / KB;
-    const bool materialise = p.logits != nullptr;
-    const bool select = p.topk > 0;
+    const bool materialise = !V41 && p.logits != nullptr;
+    const bool select = !V41 && p.topk > 0;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
@@ -231,27 +300,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u = unit_of(i, p.num_units);
                 if (u == -2) break;
                 if (u < 0) continue;
-                const Unit un = make_unit<QT>(p, u);
+                const Unit un = make_unit<QT, V41>(p, u);
                 if (un.hi_t <= un.lo_t) continue;
                 if (!(ok = mbar_wait(q_empty, (qcount & 1) ^ 1))) break;
                 ++qcount;
                 mbar_arrive_expect_tx(q_full, kN * p.D * 2);
                 for (int kb = 0; kb < nkb; ++kb)
-                    tma_load_4d(sQ + kb * kN * swz, &tmq, q_full, kb * KB, 0, un.b, un.s0);
+                {
+                    if constexpr (V41)  // q [B,S,H,D]: dims (D, H, S, B)
+                        tma_load_4d(sQ + kb * kN * swz, &tmq, q_full, kb * KB, 0, un.s0, un.b);
+                    else  // q [S,B,H,D]: dims (D, H, B, S)
+                        tma_load_4d(sQ + kb * kN * swz, &tmq, q_full, kb * KB, 0, un.b, un.s0);
+                }
                 // warm L2 with the next query tile of this CTA
                 const int un2 = unit_of(i + 1, p.num_units);
                 if (un2 >= 0) {
                     const int qt2 = p.qtiles - 1 - un2 / p.B;
                     for (int kb = 0; kb < nkb; ++kb)
-                        tma_prefetch_l2_4d(&tmq, kb * KB, 0, un2 % p.B, qt2 * QT);
+                    {
+                        if constexpr (V41)
+                            tma_prefetch_l2_4d(&tmq, kb * KB, 0, qt2 * QT, un2 % p.B);
+                        else
+                            tma_prefetch_l2_4d(&tmq, kb * KB, 0, un2 % p.B, qt2 * QT);
+                    }
                 }
-                for (int kt = un.lo_t; kt < un.hi_t; ++kt, ++kcount) {
+                for (int kt = un.lo_t; kt < un.hi_t; ++kt) {
+                    if (!tile_active<V41>(p, un, kt)) continue;
                     const int st = kcount % kStages;
                     if (!(ok = mbar_wait(k_empty + st, ((kcount / kStages) & 1) ^ 1))) break;
+                    ++kcount;
                     uint8_t* dst = sK + st * kM * p.D * 2;
                     mbar_arrive_expect_tx(k_full + st, kM * p.D * 2);
-                    for (int kb = 0; kb < nkb; ++kb)
-                        tma_load_3d(dst + kb * kM * swz, &tmk, k_full + st, kb * KB, un.b, kt * kM);
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        if constexpr (V41)  // k [B,Skv,D]: dims (D, Skv, B)
+                            tma_load_3d(dst + kb * kM * swz, &tmk, k_full + st, kb * KB, kt * kM, un.b);
+                        else  // k [Skv,B,D]: dims (D, B, Skv)
+                            tma_load_3d(dst + kb * kM * swz, &tmk, k_full + st, kb * KB, un.b, kt * kM);
+                    }
                 }
             }
         }
@@ -265,16 +350,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int u = unit_of(i, p.num_units);
                 if (u == -2) break;
                 if (u < 0) continue;
-                const Unit un = make_unit<QT>(p, u);
+                const Unit un = make_unit<QT, V41>(p, u);
                 if (un.hi_t <= un.lo_t) continue;
                 if (!(ok = mbar_wait(q_full, qcount & 1))) break;
                 ++qcount;
                 tc_fence_after();
-                for (int kt = un.lo_t; kt < un.hi_t; ++kt, ++kcount, ++tcount) {
+                for (int kt = un.lo_t; kt < un.hi_t; ++kt) {
+                    if (!tile_active<V41>(p, un, kt)) continue;
                     const int st = kcount % kStages, acc = tcount & 1;
-                    if (!(ok = mbar_wait(acc_empty + acc, ((tcount >> 1) & 1) ^ 1))) break;
+                    const uint32_t kph = (kcount / kStages) & 1, aph = ((tcount >> 1) & 1) ^ 1;
+                    ++kcount;
+                    ++tcount;
+                    if (!(ok = mbar_wait(acc_empty + acc, aph))) break;
                     tc_fence_after();
-                    if (!(ok = mbar_wait(k_full + st, (kcount / kStages) & 1))) break;
+                    if (!(ok = mbar_wait(k_full + st, kph))) break;
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(sK + st * kM * p.D * 2);
                     const uint32_t b0 = smem_u32(sQ);
@@ -305,7 +394,66 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int u = unit_of(i, p.num_units);
             if (u == -2) break;
             if (u < 0) continue;
-            const Unit un = make_unit<QT>(p, u);
+            const Unit un = make_unit<QT, V41>(p, u);
+            if constexpr (V41) {
+                // bf16 weights of the query tile, two per word (one per word at H = 1)
+                constexpr int WPER = H >= 2 ? 2 : 1;
+                uint32_t* sWp = reinterpret_cast<uint32_t*>(sW);
+                named_bar_sync(kEpiBar, kEpiThreads);
+                for (int e = etid; e < kN / WPER; e += kEpiThreads) {
+                    const int ql = (WPER * e) / H, h = (WPER * e) % H, s = un.s0 + ql;
+                    uint32_t v = 0;
+                    if (s < p.S) {
+                        const uint16_t* wr = p.w16 + ((size_t)un.b * p.S + s) * H + h;
+                        v = WPER == 2 ? (uint32_t)wr[0] | ((uint32_t)wr[1] << 16) : (uint32_t)wr[0];
+                    }
+                    sWp[e] = v;
+                }
+                named_bar_sync(kEpiBar, kEpiThreads);
+                for (int kt = un.lo_t; kt < un.hi_t; ++kt) {
+                    if (!tile_active<V41>(p, un, kt)) continue;  // written as -inf by the mask pass
+                    const int t = kt * kM + row_t;
+                    const int acc = tcount & 1;
+                    if (!(ok = mbar_wait(acc_full + acc, (tcount >> 1) & 1))) break;
+                    ++tcount;
+                    tc_fence_after();
+                    auto store16 = [&](int ql, float v) {
+                        const int s = un.s0 + ql;
+                        if (s >= p.S || t >= p.Skv) return;
+                        const size_t o = ((size_t)un.b * p.S + s) * p.Skv + t;
+                        uint16_t bits = 0xFF80u;  // -inf
+                        if (p.allowed[o]) bits = (uint16_t)(__float_as_uint(bf16_round_f(v)) >> 16);
+                        p.out16[o] = bits;
+                    };
+                    float carry = 0.f;
+#pragma unroll
+                    for (int pr = 0; pr < 4; ++pr) {
+                        uint32_t r[64];
+                        tmem_ld32(lane_addr + acc * kN + pr * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+                        tmem_ld32(lane_addr + acc * kN + pr * 64 + 32,
+                                  *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                        tmem_ld_wait();
+                        if (pr == 3) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(acc_empty + acc);
+                        }
+                        const uint32_t* wp = sWp + pr * (64 / WPER);
+                        if constexpr (H == 128) {
+                            carry += head_sum_v41<64>(r, 0, wp, p.act);
+                            if (pr & 1) {
+                                store16(pr >> 1, carry);
+                                carry = 0.f;
+                            }
+                        } else {
+#pragma unroll
+                            for (int qq = 0; qq < 64 / H; ++qq)
+                                store16(pr * (64 / H) + qq, head_sum_v41<H>(r, qq * H, wp + (qq * H) / WPER, p.act));
+                        }
+                    }
+                }
+                continue;
+            }
             const int rb = ucount & 1;
             float* rows = nullptr;
             if (select) {
@@ -407,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int u = unit_of(i, p.num_units);
             if (u == -2) break;
             if (u < 0) continue;
-            const Unit un = make_unit<QT>(p, u);
+            const Unit un = make_unit<QT, V41>(p, u);
             const int rb = ucount & 1;
             if (!(ok = mbar_wait(rows_full + rb, (ucount >> 1) & 1))) break;
             const float* rows = materialise
@@ -464,15 +612,33 @@ static int encode_maps(const ScoreLaunch& a, CUtensorMap* mq, CUtensorMap* mk) {
     return 0;
 }
 
-template <int H>
+template <int H, bool V41>
 static cudaError_t launch_h(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                             int smem, int grid) {
-    auto kern = score_fwd_kernel<H>;
+    auto kern = score_fwd_kernel<H, V41>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, a.p);
     return cudaGetLastError();
 }
+
+template <bool V41>
+static cudaError_t launch_any(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                              int smem, int grid) {
+    switch (a.p.H) {
+        case 1: return launch_h<1, V41>(a, mq, mk, smem, grid);
+        case 2: return launch_h<2, V41>(a, mq, mk, smem, grid);
+        case 4: return launch_h<4, V41>(a, mq, mk, smem, grid);
+        case 8: return launch_h<8, V41>(a, mq, mk, smem, grid);
+        case 16: return launch_h<16, V41>(a, mq, mk, smem, grid);
+        case 32: return launch_h<32, V41>(a, mq, mk, smem, grid);
+        case 64: return launch_h<64, V41>(a, mq, mk, smem, grid);
+        case 128: return launch_h<128, V41>(a, mq, mk, smem, grid);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int score_query_tile(int H) { return kN / H; }
 
 size_t score_scratch_bytes(int64_t S, int64_t Skv, int H, int num_sms) {
     (void)S;
@@ -496,18 +662,45 @@ int score_fwd_launch(ScoreLaunch& a) {
     // at least 120 KB so that one CTA (and its 512 TMEM columns) owns each SM
     int smem = (int)smem_layout(p.D).total;
     if (smem < 120 * 1024) smem = 120 * 1024;
-    cudaError_t e;
-    switch (p.H) {
-        case 1: e = launch_h<1>(a, mq, mk, smem, grid); break;
-        case 2: e = launch_h<2>(a, mq, mk, smem, grid); break;
-        case 4: e = launch_h<4>(a, mq, mk, smem, grid); break;
-        case 8: e = launch_h<8>(a, mq, mk, smem, grid); break;
-        case 16: e = launch_h<16>(a, mq, mk, smem, grid); break;
-        case 32: e = launch_h<32>(a, mq, mk, smem, grid); break;
-        case 64: e = launch_h<64>(a, mq, mk, smem, grid); break;
-        case 128: e = launch_h<128>(a, mq, mk, smem, grid); break;
-        default: return -2;
-    }
+    if (p.H < 1 || p.H > 128 || (p.H & (p.H - 1))) return -2;
+    const cudaError_t e = launch_any<false>(a, mq, mk, smem, grid);
+    a.launched = grid;
+    return e == cudaSuccess ? 0 : -1;
+}
+
+// V4.1: q [B,S,H,D], k [B,Skv,D].  Key tiles come from p.tilemap, built by the
+// mask pass, which also wrote -inf for every block it marked empty.
+int score_v41_launch(ScoreLaunch& a) {
+    ScoreParams& p = a.p;
+    if (p.H < 1 || p.H > 128 || (p.H & (p.H - 1))) return -2;
+    const int QT = kN / p.H;
+    p.swz = (p.D % 64 == 0) ? 128 : (p.D % 32 == 0 ? 64 : 32);
+    p.qtiles = (p.S + QT - 1) / QT;
+    p.num_units = p.B * p.qtiles;
+    p.Skv_pad = (p.Skv + kM - 1) / kM * kM;
+    p.ntk = (p.Skv + kM - 1) / kM;
+    const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+    if (grid <= 0) return 0;
+    const int swz = p.swz, KB = swz / 2;
+    const CUtensorMapSwizzle sw = swz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B
+                                  : swz == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                              : CU_TENSOR_MAP_SWIZZLE_32B;
+    const int H = p.H, D = p.D, B = p.B;
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUtensorMap mq, mk;
+    cuuint64_t qdim[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)p.S, (cuuint64_t)B};
+    cuuint64_t qstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)p.S * H * D * 2};
+    cuuint32_t qbox[4] = {(cuuint32_t)KB, (cuuint32_t)H, (cuuint32_t)QT, 1};
+    if (encode_tiled(&mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void*)a.q, qdim, qstr, qbox, es, sw))
+        return -1;
+    cuuint64_t kdim[3] = {(cuuint64_t)D, (cuuint64_t)p.Skv, (cuuint64_t)B};
+    cuuint64_t kstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Skv * D * 2};
+    cuuint32_t kbox[3] = {(cuuint32_t)KB, (cuuint32_t)kM, 1};
+    if (encode_tiled(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.k, kdim, kstr, kbox, es, sw))
+        return -1;
+    int smem = (int)smem_layout(p.D).total;
+    if (smem < 120 * 1024) smem = 120 * 1024;
+    const cudaError_t e = launch_any<true>(a, mq, mk, smem, grid);
     a.launched = grid;
     return e == cudaSuccess ? 0 : -1;
 }

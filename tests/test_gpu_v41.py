@@ -1,0 +1,129 @@
+"""GPU parity of the V4.1 bf16-rounded scorer (lidx_indexer_scores_v41)
+against the CPU oracle: exact on integer-valued inputs; within one bf16 ulp on
+>= 99.9% of visible entries otherwise, the rest within the bound of a head's
+GEMM result rounding across a bf16 tie; -inf exactly where not visible."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_top_tcgen05_gb300 as lidx
+import workloads
+from parity import bf16_ulp_diff
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from sparse_attention_top_tcgen05_gb300 import build
+
+    build.build()
+    lidx.lib()
+    yield
+    assert lidx.lidx_device_status() == 0
+
+
+def run(q, k, w, allowed, act="relu"):
+    out = lidx.lidx_indexer_scores_v41(q.to(DEV), k.to(DEV), w.to(DEV), allowed.to(DEV), act=act)
+    torch.cuda.synchronize()
+    assert lidx.lidx_device_status() == 0
+    return out.float().cpu().numpy()
+
+
+def flip_bound(q, k, w, rows=None):
+    """Per-entry bound on the score change when the fp32 GEMM result of one or
+    two heads lies on the other side of a bf16 tie from the exact one (6 ulp of
+    the largest weighted term), plus fp32 reduction error and final rounding."""
+    B, S, H, D = q.shape
+    r = np.arange(B * S) if rows is None else np.asarray(rows)
+    qf = q.float().numpy().astype(np.float64).reshape(B * S, H, D)[r]
+    wf = w.float().numpy().astype(np.float64).reshape(B * S, H)[r]
+    kf = k.float().numpy().astype(np.float64)
+    bidx = r // S
+    out = np.empty((r.size, kf.shape[1]))
+    ulp = lambda v: np.exp2(np.floor(np.log2(np.maximum(v, 1e-38))) - 7)
+    for i in range(r.size):
+        x = qf[i] @ kf[bidx[i]].T                 # [H, Skv]
+        term = np.abs(x * wf[i][:, None])
+        tot = np.abs((x * wf[i][:, None]).sum(0))
+        out[i] = 6 * ulp(term.max(0)) + 2 * ulp(tot) + 64 * 2.0 ** -24 * term.sum(0)
+    return out
+
+
+def check(got, ref, allowed, exact=False, bound=None):
+    al = allowed.numpy().reshape(got.shape).astype(bool)
+    assert np.isneginf(got[~al]).all(), "invisible entries must be -inf"
+    assert np.isfinite(got[al]).all()
+    if exact:
+        assert np.array_equal(got[al], ref[al])
+    elif al.any():
+        ulp = bf16_ulp_diff(got[al], ref[al])
+        assert (ulp <= 1).mean() >= 0.999, (ulp <= 1).mean()
+        if bound is not None and (ulp > 1).any():
+            err = np.abs(got[al].astype(np.float64) - ref[al])
+            bad = (ulp > 1) & (err > bound[al])
+            assert not bad.any(), (err[bad][:5], bound[al][bad][:5])
+
+
+@pytest.mark.parametrize("H,D", [(4, 16), (64, 128), (8, 32), (128, 64)])
+def test_integer_inputs_bit_exact(H, D):
+    B, S, Skv = 2, 160, 300
+    q, k, w = workloads.integer_inputs(B, S, Skv, H, 16, seed=H)
+    if D > 16:  # keep |q.k| small and every rounding exact: zero the extra dims
+        q = torch.cat([q, torch.zeros(*q.shape[:-1], D - 16, dtype=q.dtype)], -1)
+        k = torch.cat([k, torch.zeros(*k.shape[:-1], D - 16, dtype=k.dtype)], -1)
+    q = q.permute(1, 0, 2, 3).contiguous()
+    k = k.permute(1, 0, 2).contiguous()
+    w = w.permute(1, 0, 2).contiguous().to(torch.bfloat16)
+    allowed = torch.from_numpy(np.random.default_rng(H).random((B, S, Skv)) < 0.3)
+    got = run(q, k, w, allowed).reshape(B * S, Skv)
+    ref = oracle.scores_v41_rows(q, k, w, allowed)
+    check(got, ref, allowed, exact=True)
+
+
+def test_packed_documents_full_size_sampled():
+    wl = workloads.WORKLOADS["v41_packed"]
+    q, k, w, allowed = workloads.v41_inputs(wl, 0)
+    got = run(q, k, w, allowed).reshape(wl.B * wl.S, wl.Skv)
+    rows = workloads.sample_rows(wl.B, wl.S, 61, 5)
+    ref = oracle.scores_v41_rows(q, k, w, allowed, rows=rows)
+    check(got[rows], ref, allowed.reshape(wl.B * wl.S, wl.Skv)[rows],
+          bound=flip_bound(q, k, w, rows=rows))
+    # every masked entry of every row is -inf, every visible one finite
+    al = allowed.numpy().reshape(wl.B * wl.S, wl.Skv)
+    assert np.isneginf(got[~al]).all() and np.isfinite(got[al]).all()
+
+
+@pytest.mark.parametrize("B,S,Skv,H,D,density", [
+    (1, 300, 257, 64, 128, 0.5),   # ragged key tiles, Skv not a multiple of 4
+    (2, 77, 1000, 16, 64, 0.05),
+    (1, 64, 130, 1, 16, 0.9),
+    (3, 40, 64, 32, 32, 1.0),
+])
+def test_shapes_random_visibility(B, S, Skv, H, D, density):
+    g = np.random.default_rng(S + Skv)
+    q = workloads.to_bf16(g.standard_normal((B, S, H, D)).astype(np.float32) / np.sqrt(D))
+    k = workloads.to_bf16(g.standard_normal((B, Skv, D)).astype(np.float32) / np.sqrt(D))
+    w = workloads.to_bf16(g.standard_normal((B, S, H)).astype(np.float32) / np.sqrt(H))
+    allowed = torch.from_numpy(g.random((B, S, Skv)) < density)
+    bnd = flip_bound(q, k, w)
+    got = run(q, k, w, allowed).reshape(B * S, Skv)
+    check(got, oracle.scores_v41_rows(q, k, w, allowed), allowed, bound=bnd)
+    gi = run(q, k, w, allowed, act="identity").reshape(B * S, Skv)
+    check(gi, oracle.scores_v41_rows(q, k, w, allowed, act="identity"), allowed, bound=bnd)
+
+
+def test_all_false_and_all_true():
+    g = np.random.default_rng(8)
+    B, S, Skv, H, D = 1, 50, 200, 8, 32
+    q = workloads.to_bf16(g.standard_normal((B, S, H, D)).astype(np.float32))
+    k = workloads.to_bf16(g.standard_normal((B, Skv, D)).astype(np.float32))
+    w = workloads.to_bf16(g.standard_normal((B, S, H)).astype(np.float32))
+    none = torch.zeros(B, S, Skv, dtype=torch.bool)
+    assert np.isneginf(run(q, k, w, none)).all()
+    full = torch.ones(B, S, Skv, dtype=torch.bool)
+    check(run(q, k, w, full).reshape(B * S, Skv), oracle.scores_v41_rows(q, k, w, full), full,
+          bound=flip_bound(q, k, w))
