@@ -280,17 +280,40 @@ int lidx_indexer_bwd(const void* q, const void* k, const float* w, const int32_t
                      const float* grad_scores, int64_t B, int64_t S, int64_t Skv, int H, int D,
                      int compress_ratio, int topk, int act, int grad_dtype, void* dq, void* dk,
                      float* dw, void* workspace, size_t workspace_bytes, void* stream) {
-    (void)compress_ratio;
-    (void)act;
-    (void)grad_dtype;
     (void)workspace;
     (void)workspace_bytes;
-    (void)stream;
-    if (!q || !k || !w || !idx || !grad_scores || !dq || !dk || !dw) return LIDX_ERR_NULL;
+    if (!q || !w || !idx || !grad_scores || !dq || !dw || (Skv > 0 && (!k || !dk)))
+        return LIDX_ERR_NULL;
     int rc = check_dims(B, S, Skv, H, D);
     if (rc) return rc;
-    if (topk < 1) return LIDX_ERR_SHAPE;
-    return LIDX_ERR_UNSUPPORTED;
+    if (topk < 1 || topk > (1 << 20) || compress_ratio < 1 || (act != 0 && act != 1))
+        return LIDX_ERR_SHAPE;
+    if (grad_dtype != 0) return LIDX_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(w) || !aligned16(dq) || !aligned16(dk) ||
+        !aligned16(dw))
+        return LIDX_ERR_ALIGN;
+    const int sms = device_sms(true);
+    if (sms <= 0) return LIDX_ERR_NO_DEVICE;
+    BwdLaunch a;
+    a.q = q;
+    a.k = k;
+    a.w = w;
+    a.idx = idx;
+    a.grad = grad_scores;
+    a.B = (int)B;
+    a.S = (int)S;
+    a.Skv = (int)Skv;
+    a.H = H;
+    a.D = D;
+    a.ratio = compress_ratio;
+    a.topk = topk;
+    a.act = act;
+    a.dq = (float*)dq;
+    a.dk = (float*)dk;
+    a.dw = dw;
+    a.stream = (cudaStream_t)stream;
+    a.num_sms = sms;
+    return bwd_launch(a) == cudaSuccess ? LIDX_OK : LIDX_ERR_CUDA;
 }
 
 }  // extern "C"

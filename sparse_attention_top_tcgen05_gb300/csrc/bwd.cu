@@ -1,0 +1,227 @@
+// bwd.cu -- backward of the V4 indexer through the selected entries
+// ("tilelang_indexer" page, V4IndexerFunction.backward(grad_scores,
+// grad_indices); grad_indices carries no gradient).
+//
+// For query row (b,s) and selected slot j with key t = idx[j] inside the row's
+// causal range and g = grad[j], with x_h = q[s,b,h,:] . k[t,b,:]:
+//     dw[s,b,h]   += g * act(x_h)
+//     c_h          = g * w[s,b,h] * act'(x_h)          (ReLU'(0) = 0)
+//     dq[s,b,h,:] += c_h * k[t,b,:]
+//     dk[t,b,:]   += sum_h c_h * q[s,b,h,:]
+//
+// One CTA per query row.  The row's queries stay in shared memory; its
+// selected keys are gathered in chunks of J.  Per chunk three small
+// contractions run on the CUDA cores with register tiles of four:
+//     X [H x J]  = Q [H x D] . Kc^T        (then dw and C = g*w*act'(x))
+//     dq[H x D] += C [H x J] . Kc [J x D]  (accumulated in registers)
+//     dKc[J x D] = C^T [J x H] . Q [H x D] (scatter-added to dk)
+// dq and dw are written once per row; dk is cleared by the caller-side
+// launcher and accumulated with atomics (order-dependent in the last bits).
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace lidx {
+
+constexpr int kBwdThreads = 256;
+constexpr int kBwdJ = 64;  // selected keys per chunk
+
+__device__ __forceinline__ float bf16_to_f(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+
+template <int H>
+__global__ void __launch_bounds__(kBwdThreads)
+    bwd_rows_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                    const float* __restrict__ w, const int32_t* __restrict__ idx,
+                    const float* __restrict__ grad, int B, int S, int Skv, int D, int ratio,
+                    int topk, int act, float* __restrict__ dq, float* __restrict__ dk,
+                    float* __restrict__ dw) {
+    extern __shared__ __align__(16) float sm[];
+    const int DP = D + 4;                      // padded row stride (keeps 16-byte alignment)
+    float* qs = sm;                            // [H][DP]
+    float* kc = qs + H * DP;                   // [J][DP]   gathered keys
+    float* kT = kc + kBwdJ * DP;               // [D][J+4]  the same keys transposed
+    float* cs = kT + D * (kBwdJ + 4);          // [H][J+4]  C = g*w*act'(x)
+    float* ws = cs + H * (kBwdJ + 4);          // [H]
+    float* dws = ws + H;                       // [H]
+    float* gs = dws + H;                       // [J]
+    int* ts = reinterpret_cast<int*>(gs + kBwdJ);  // [J]   key, or -1
+    const int tid = threadIdx.x;
+    const int D4 = D / 4;
+    constexpr int JP = kBwdJ + 4;
+    // fixed work split of the three contractions
+    const int nX = H * (kBwdJ / 4);            // groups (h, 4 keys)
+    const int nQ = H * D4;                     // groups (h, 4 dims)
+    const int nK = kBwdJ * D4;                 // groups (key, 4 dims)
+    constexpr int MAXQ = (H * 32 + kBwdThreads - 1) / kBwdThreads;  // D <= 128
+
+    for (int r = blockIdx.x; r < B * S; r += gridDim.x) {
+        const int b = r / S, s = r % S;
+        const long long ke_ll = (long long)(s + 1) / ratio;
+        const int ke = (int)(ke_ll < Skv ? ke_ll : Skv);
+        __syncthreads();  // previous row done with shared memory
+        for (int e = tid; e < H * D; e += kBwdThreads) {
+            const int h = e / D, d = e % D;
+            qs[h * DP + d] = bf16_to_f(q[(((size_t)s * B + b) * H + h) * D + d]);
+        }
+        for (int h = tid; h < H; h += kBwdThreads) {
+            ws[h] = w[((size_t)s * B + b) * H + h];
+            dws[h] = 0.f;
+        }
+        float accq[MAXQ][4];
+#pragma unroll
+        for (int i = 0; i < MAXQ; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) accq[i][c] = 0.f;
+
+        const int32_t* irow = idx + (size_t)r * topk;
+        const float* grow = grad + (size_t)r * topk;
+        for (int j0 = 0; j0 < topk; j0 += kBwdJ) {
+            __syncthreads();  // previous chunk done with kc/kT/cs
+            for (int j = tid; j < kBwdJ; j += kBwdThreads) {
+                const int slot = j0 + j;
+                int t = slot < topk ? irow[slot] : -1;
+                if (t < 0 || t >= ke) t = -1;  // padding or outside the causal range
+                ts[j] = t;
+                gs[j] = t >= 0 ? grow[slot] : 0.f;
+            }
+            __syncthreads();
+            for (int e = tid; e < kBwdJ * D; e += kBwdThreads) {
+                const int j = e / D, d = e % D;
+                const int t = ts[j];
+                const float v = t >= 0 ? bf16_to_f(k[((size_t)t * B + b) * D + d]) : 0.f;
+                kc[j * DP + d] = v;
+                kT[d * JP + j] = v;
+            }
+            __syncthreads();
+            // X and C: thread group (h, four keys)
+            for (int gi = tid; gi < nX; gi += kBwdThreads) {
+                const int h = gi / (kBwdJ / 4), j4 = (gi % (kBwdJ / 4)) * 4;
+                float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
+                const float* qh = qs + h * DP;
+                for (int d = 0; d < D; ++d) {
+                    const float qv = qh[d];
+                    const float4 kv = *reinterpret_cast<const float4*>(kT + d * JP + j4);
+                    x0 = fmaf(qv, kv.x, x0);
+                    x1 = fmaf(qv, kv.y, x1);
+                    x2 = fmaf(qv, kv.z, x2);
+                    x3 = fmaf(qv, kv.w, x3);
+                }
+                const float xs[4] = {x0, x1, x2, x3};
+                float dwp = 0.f, cv[4];
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float g = gs[j4 + c];
+                    const float x = xs[c];
+                    const float a = act == 0 ? fmaxf(x, 0.f) : x;
+                    const float da = act == 0 ? (x > 0.f ? 1.f : 0.f) : 1.f;
+                    dwp = fmaf(g, a, dwp);
+                    cv[c] = g * ws[h] * da;
+                }
+                *reinterpret_cast<float4*>(cs + h * JP + j4) = make_float4(cv[0], cv[1], cv[2], cv[3]);
+                atomicAdd(&dws[h], dwp);
+            }
+            __syncthreads();
+            // dq += C . Kc: thread group (h, four dims), kept in registers across chunks
+#pragma unroll
+            for (int i = 0; i < MAXQ; ++i) {
+                const int gi = tid + i * kBwdThreads;
+                if (gi < nQ) {
+                    const int h = gi / D4, d4 = (gi % D4) * 4;
+                    const float* ch = cs + h * JP;
+                    float a0 = accq[i][0], a1 = accq[i][1], a2 = accq[i][2], a3 = accq[i][3];
+                    for (int j = 0; j < kBwdJ; ++j) {
+                        const float cvj = ch[j];
+                        const float4 kv = *reinterpret_cast<const float4*>(kc + j * DP + d4);
+                        a0 = fmaf(cvj, kv.x, a0);
+                        a1 = fmaf(cvj, kv.y, a1);
+                        a2 = fmaf(cvj, kv.z, a2);
+                        a3 = fmaf(cvj, kv.w, a3);
+                    }
+                    accq[i][0] = a0;
+                    accq[i][1] = a1;
+                    accq[i][2] = a2;
+                    accq[i][3] = a3;
+                }
+            }
+            // dk[t] += C^T . Q: thread group (key, four dims)
+            for (int gi = tid; gi < nK; gi += kBwdThreads) {
+                const int j = gi / D4, d4 = (gi % D4) * 4;
+                const int t = ts[j];
+                if (t < 0) continue;
+                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+                for (int h = 0; h < H; ++h) {
+                    const float cvh = cs[h * JP + j];
+                    const float4 qv = *reinterpret_cast<const float4*>(qs + h * DP + d4);
+                    a0 = fmaf(cvh, qv.x, a0);
+                    a1 = fmaf(cvh, qv.y, a1);
+                    a2 = fmaf(cvh, qv.z, a2);
+                    a3 = fmaf(cvh, qv.w, a3);
+                }
+                float* o = dk + ((size_t)t * B + b) * D + d4;
+                atomicAdd(o + 0, a0);
+                atomicAdd(o + 1, a1);
+                atomicAdd(o + 2, a2);
+                atomicAdd(o + 3, a3);
+            }
+        }
+        // dq and dw of this row
+#pragma unroll
+        for (int i = 0; i < MAXQ; ++i) {
+            const int gi = tid + i * kBwdThreads;
+            if (gi < nQ) {
+                const int h = gi / D4, d4 = (gi % D4) * 4;
+                *reinterpret_cast<float4*>(dq + (((size_t)s * B + b) * H + h) * D + d4) =
+                    make_float4(accq[i][0], accq[i][1], accq[i][2], accq[i][3]);
+            }
+        }
+        __syncthreads();
+        for (int h = tid; h < H; h += kBwdThreads) dw[((size_t)s * B + b) * H + h] = dws[h];
+    }
+}
+
+static size_t bwd_smem(int H, int D) {
+    const int DP = D + 4, JP = kBwdJ + 4;
+    return sizeof(float) * ((size_t)H * DP + (size_t)kBwdJ * DP + (size_t)D * JP + (size_t)H * JP +
+                            2 * (size_t)H + kBwdJ) +
+           sizeof(int) * kBwdJ;
+}
+
+template <int H>
+static cudaError_t bwd_h(const BwdLaunch& a) {
+    const size_t smem = bwd_smem(H, a.D);
+    auto kern = bwd_rows_kernel<H>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBwdThreads, smem);
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)a.num_sms * per_sm;
+    const int64_t rows = (int64_t)a.B * a.S;
+    if (grid > rows) grid = rows;
+    kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(
+        (const uint16_t*)a.q, (const uint16_t*)a.k, a.w, a.idx, a.grad, a.B, a.S, a.Skv, a.D, a.ratio,
+        a.topk, a.act, a.dq, a.dk, a.dw);
+    return cudaGetLastError();
+}
+
+cudaError_t bwd_launch(const BwdLaunch& a) {
+    // dk is a sum over rows: clear it first (dq and dw are written whole)
+    cudaError_t e = cudaMemsetAsync(a.dk, 0, sizeof(float) * (size_t)a.Skv * a.B * a.D, a.stream);
+    if (e != cudaSuccess) return e;
+    if ((int64_t)a.B * a.S == 0) return cudaSuccess;
+    switch (a.H) {
+        case 1: return bwd_h<1>(a);
+        case 2: return bwd_h<2>(a);
+        case 4: return bwd_h<4>(a);
+        case 8: return bwd_h<8>(a);
+        case 16: return bwd_h<16>(a);
+        case 32: return bwd_h<32>(a);
+        case 64: return bwd_h<64>(a);
+        case 128: return bwd_h<128>(a);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace lidx

@@ -58,6 +58,22 @@ cudaError_t extract_launch(const float* logits, const int32_t* idx, int64_t rows
 cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, int ratio,
                              const int32_t* ks, const int32_t* ke, int topk, int32_t* out_idx,
                              float* out_sc, cudaStream_t stream);
+// backward through the selected entries (bwd.cu)
+struct BwdLaunch {
+    const void* q;
+    const void* k;
+    const float* w;
+    const int32_t* idx;
+    const float* grad;
+    int B, S, Skv, H, D, ratio, topk, act;
+    float* dq;
+    float* dk;
+    float* dw;
+    cudaStream_t stream;
+    int num_sms;
+};
+cudaError_t bwd_launch(const BwdLaunch& a);
+
 cudaError_t pad_launch(int64_t n, int32_t* idx, float* sc, cudaStream_t stream);
 
 // per-TU status readers (see LIDX_STATUS_READER): value, or -1 on a CUDA error

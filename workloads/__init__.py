@@ -173,6 +173,8 @@ def random_selection(B: int, S: int, Skv: int, topk: int, counts, seed: int = 0)
         keys = g.random((S, Skv), dtype=np.float32)
         keys[cols >= n[:, None]] = 2.0  # keys past the row's count sort last
         order = np.argsort(keys, axis=1, kind="stable")[:, :topk].astype(np.int32)
+        if order.shape[1] < topk:  # fewer keys than slots: pad the tail
+            order = np.pad(order, ((0, 0), (0, topk - order.shape[1])), constant_values=-1)
         cnt = np.minimum(n, topk)
         valid = np.arange(topk)[None, :] < cnt[:, None]
         idx[b] = np.where(valid, order, -1)
