@@ -160,11 +160,18 @@ def max_over_ranks(x, world):
 
 
 # ------------------------------------------------------------------ CPU oracle
+_CPU_INPUTS = {}
+
+
 def cpu_oracle_sample(wl, stride, seed=0):
     """Time the oracle (as it stands) on every `stride`-th row of the workload."""
     import oracle
 
-    q, k, w = workloads.v4_inputs(wl, seed)
+    key = (wl.name, wl.B, wl.S, wl.Skv, seed)
+    if key not in _CPU_INPUTS:
+        _CPU_INPUTS.clear()
+        _CPU_INPUTS[key] = workloads.v4_inputs(wl, seed)
+    q, k, w = _CPU_INPUTS[key]
     rows = workloads.sample_rows(wl.B, wl.S, stride, 0)
     ks, ke = oracle.causal_ranges(wl.S, wl.Skv, wl.ratio)
     pairs = int(sum(ke[r % wl.S] - ks[r % wl.S] for r in rows))
@@ -253,6 +260,47 @@ def side_workloads(lidx, pk):
                      "hbm_gbs": alg_bytes / ms / 1e6, "hbm_frac": alg_bytes / ms / 1e6 / pk["hbm_gbs"],
                      "l2": "256 MB flush before each launch"}
     del q, k, w, idx, sc, lg
+
+    # V4.1 packed documents: HBM-bound (q, allowed read; bf16 scores written)
+    wl = workloads.WORKLOADS["v41_packed"]
+    q, k, w, allowed = [t.cuda() for t in workloads.v41_inputs(wl, 0)]
+    out16 = torch.empty(wl.B, wl.S, wl.Skv, dtype=torch.bfloat16, device="cuda")
+    wsb = lidx.lidx_workspace_bytes(lidx.OP_SCORES_V41, wl.B, wl.S, wl.Skv, wl.H, wl.D)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    fn = lambda: lidx.lidx_indexer_scores_v41(q, k, w, allowed, out=out16, workspace=ws)
+    for _ in range(3):
+        fn()
+    ts = []
+    for _ in range(10):
+        flush.zero_()
+        ts.append(time_steps(fn, 1, stream))
+    ms = statistics.median(ts)
+    vis = int(allowed.sum().item())
+    alg_bytes = (q.numel() * 2 + k.numel() * 2 + w.numel() * 2 + allowed.numel() + out16.numel() * 2)
+    out["v41_packed"] = {"ms": ms, "hbm_gbs": alg_bytes / ms / 1e6,
+                         "hbm_frac": alg_bytes / ms / 1e6 / pk["hbm_gbs"],
+                         "algorithmic_bytes": alg_bytes, "visible_pairs": vis,
+                         "visible_pair_tflops": vis * 2.0 * wl.H * wl.D / ms / 1e9,
+                         "launches": 2, "l2": "256 MB flush before each call"}
+    del q, k, w, allowed, out16, ws
+
+    # backward through the selected entries (selection: the forward's own top-k)
+    wl = workloads.WORKLOADS["bwd"]
+    q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
+    idx, _, _ = lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk)
+    grad = workloads.grad_scores(wl.B, wl.S, wl.topk, 0).cuda()
+    outs = (torch.empty(wl.S, wl.B, wl.H, wl.D, device="cuda"), torch.empty(wl.Skv, wl.B, wl.D, device="cuda"),
+            torch.empty(wl.S, wl.B, wl.H, device="cuda"))
+    fn = lambda: lidx.lidx_indexer_bwd(q, k, w, idx, grad, wl.ratio, out=outs)
+    for _ in range(2):
+        fn()
+    ms = time_steps(fn, 3, stream)
+    sel = int((idx >= 0).sum().item())
+    fl = sel * 6.0 * wl.H * wl.D
+    out["bwd"] = {"ms": ms, "selected_pairs": sel, "tflops": fl / ms / 1e9,
+                  "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
+                  "kernel": "bwd_rows_kernel<64> (CUDA cores)", "launches": 2}
+    del q, k, w, idx, grad, outs
     return out
 
 
