@@ -8,7 +8,7 @@
 
 #include <mutex>
 
-#include "../../include/lidx.h"
+#include "lidx.h"
 #include "kernels.h"
 #include "topk.cuh"
 

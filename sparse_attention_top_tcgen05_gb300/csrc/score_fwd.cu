@@ -36,14 +36,16 @@ namespace lidx {
 
 constexpr int kN = 256;            // UMMA N: query x head columns per tile
 constexpr int kM = 128;            // UMMA M: keys per tile
-constexpr int kStages = 3;         // key-tile ring depth
-constexpr int kEpiWarps = 4;
+constexpr int kStages = 2;         // key-tile ring depth
+constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, 128 columns each
 constexpr int kTopkWarps = 8;
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kTopkThreads = 32 * kTopkWarps;
 constexpr int kThreads = 64 + kEpiThreads + kTopkThreads;
 constexpr int kEpiBar = 1;         // named barrier id of the epilogue group
-constexpr int kTopkBar = 2;        // named barrier id of the top-k group
+constexpr int kTopkBar = 2;        // named barrier ids of the two selection groups: 2, 3
+constexpr int kTopkGroups = 2;     // rows selected concurrently
+constexpr int kTopkGroupThreads = kTopkThreads / kTopkGroups;
 
 struct Unit {
     int b, s0, qt;
@@ -146,7 +148,7 @@ __host__ __device__ inline SmemLayout smem_layout(int D) {
     L.range_off = o;
     o += 2 * kN * 4;
     L.topk_off = o;
-    o += (uint32_t)((sizeof(TopkSmem) + 15) / 16 * 16);
+    o += (uint32_t)(kTopkGroups * ((sizeof(TopkSmem) + 15) / 16 * 16));
     L.bar_off = o;
     o += 24 * 8;
     L.tmem_off = o;
@@ -157,29 +159,49 @@ __host__ __device__ inline SmemLayout smem_layout(int D) {
 
 // Weighted head reduction of one query's H accumulator columns held in
 // registers r[c0 .. c0+H) (c0 compile time): sum_h w[h] * act(x[h]).
+// Weighted head sum of HH consecutive columns starting at c0 of a 32-column
+// chunk held in registers (c0 is a constant once the caller's loops unroll).
+template <int HH>
+__device__ __forceinline__ float head_sum_at(const uint32_t (&r)[32], int c0, const float* w, int act) {
+    if constexpr (HH >= 4) {
+        const float4* w4 = reinterpret_cast<const float4*>(w);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int h = 0; h < HH; h += 4) {
+            const float4 wv = w4[h / 4];
+            a0 = fmaf(wv.x, act_f(__uint_as_float(r[c0 + h]), act), a0);
+            a1 = fmaf(wv.y, act_f(__uint_as_float(r[c0 + h + 1]), act), a1);
+            a2 = fmaf(wv.z, act_f(__uint_as_float(r[c0 + h + 2]), act), a2);
+            a3 = fmaf(wv.w, act_f(__uint_as_float(r[c0 + h + 3]), act), a3);
+        }
+        return (a0 + a1) + (a2 + a3);
+    } else {
+        float acc = 0.f;
+#pragma unroll
+        for (int h = 0; h < HH; ++h) acc = fmaf(w[h], act_f(__uint_as_float(r[c0 + h]), act), acc);
+        return acc;
+    }
+}
+
 template <int H, int C0, int NR>
 __device__ __forceinline__ float head_sum(const uint32_t (&r)[NR], const float* w, int act) {
     if constexpr (H >= 4) {
+        // four independent FMA chains; weights come four at a time from shared memory
         const float4* w4 = reinterpret_cast<const float4*>(w);
-        uint64_t a0 = 0, a1 = 0;  // two packed accumulators = four independent chains
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int h = 0; h < H; h += 4) {
             const float4 wv = w4[h / 4];
-            float x0 = __uint_as_float(r[C0 + h]), x1 = __uint_as_float(r[C0 + h + 1]);
-            float x2 = __uint_as_float(r[C0 + h + 2]), x3 = __uint_as_float(r[C0 + h + 3]);
-            if (act == 0) {
-                x0 = fmaxf(x0, 0.f);
-                x1 = fmaxf(x1, 0.f);
-                x2 = fmaxf(x2, 0.f);
-                x3 = fmaxf(x3, 0.f);
-            }
-            a0 = fma2(pack2(x0, x1), pack2(wv.x, wv.y), a0);
-            a1 = fma2(pack2(x2, x3), pack2(wv.z, wv.w), a1);
+            const float x0 = act_f(__uint_as_float(r[C0 + h]), act);
+            const float x1 = act_f(__uint_as_float(r[C0 + h + 1]), act);
+            const float x2 = act_f(__uint_as_float(r[C0 + h + 2]), act);
+            const float x3 = act_f(__uint_as_float(r[C0 + h + 3]), act);
+            a0 = fmaf(wv.x, x0, a0);
+            a1 = fmaf(wv.y, x1, a1);
+            a2 = fmaf(wv.z, x2, a2);
+            a3 = fmaf(wv.w, x3, a3);
         }
-        float p0, p1, p2, p3;
-        unpack2(a0, p0, p1);
-        unpack2(a1, p2, p3);
-        return (p0 + p1) + (p2 + p3);
+        return (a0 + a1) + (a2 + a3);
     } else {
         float acc = 0.f;
 #pragma unroll
@@ -248,7 +270,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sW = (float*)(smem + L.w_off);
     int* sLo = (int*)(smem + L.range_off);
     int* sHi = sLo + kN;
-    TopkSmem& sT = *(TopkSmem*)(smem + L.topk_off);
     uint64_t* bars = (uint64_t*)(smem + L.bar_off);
     uint64_t* q_full = bars + 0;
     uint64_t* q_empty = bars + 1;
@@ -344,6 +365,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kM, kN);
+            // Every descriptor the tile loop needs is built once per CTA, exactly as
+            // the per-step formula builds it (address + offset, then masked).
+            const int nk = p.D / 16;
+            uint64_t ad[kStages][8], bd[8];
+            {
+                const uint32_t a0 = smem_u32(sK), stage = (uint32_t)(kM * p.D * 2), b0 = smem_u32(sQ);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int kb = (k * 16) / KB, koff = ((k * 16) % KB) * 2;
+                    const uint32_t ao = (uint32_t)(kb * kM * swz + koff);
+#pragma unroll
+                    for (int j = 0; j < kStages; ++j) ad[j][k] = smem_desc_kmajor(a0 + j * stage + ao, swz);
+                    bd[k] = smem_desc_kmajor(b0 + (uint32_t)(kb * kN * swz + koff), swz);
+                }
+            }
             int kcount = 0, tcount = 0, qcount = 0;
             bool ok = true;
             for (int i = 0; ok; ++i) {
@@ -365,14 +401,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     if (!(ok = mbar_wait(k_full + st, kph))) break;
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sK + st * kM * p.D * 2);
-                    const uint32_t b0 = smem_u32(sQ);
                     const uint32_t d = tmem_base + acc * kN;
-                    for (int k = 0; k < p.D / 16; ++k) {
-                        const int kb = (k * 16) / KB, koff = ((k * 16) % KB) * 2;
-                        const uint64_t ad = smem_desc_kmajor(a0 + kb * kM * swz + koff, swz);
-                        const uint64_t bd = smem_desc_kmajor(b0 + kb * kN * swz + koff, swz);
-                        umma_f16(d, ad, bd, idesc, k > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        uint64_t a = ad[0][k];
+#pragma unroll
+                        for (int j = 1; j < kStages; ++j) a = st == j ? ad[j][k] : a;
+                        if (k < nk) umma_f16(d, a, bd[k], idesc, k > 0 ? 1u : 0u);
                     }
                     umma_commit(k_empty + st);
                     umma_commit(acc_full + acc);
@@ -384,6 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // --------------------------------------------------------- epilogue
         const int etid = threadIdx.x - 64;
         const int quad = warp & 3;           // TMEM lane quadrant this warp may read
+        const int half = (warp - 2) >> 2;    // which 128 of the 256 accumulator columns
+        constexpr int QH = QT / 2;           // queries per half (H <= 128)
         const int row_t = quad * 32 + lane;  // key within the tile
         const float ninf = __int_as_float(0xff800000);
         const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
@@ -425,30 +462,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (p.allowed[o]) bits = (uint16_t)(__float_as_uint(bf16_round_f(v)) >> 16);
                         p.out16[o] = bits;
                     };
-                    float carry = 0.f;
+                    float run = 0.f;
 #pragma unroll
-                    for (int pr = 0; pr < 4; ++pr) {
-                        uint32_t r[64];
-                        tmem_ld32(lane_addr + acc * kN + pr * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                        tmem_ld32(lane_addr + acc * kN + pr * 64 + 32,
-                                  *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(lane_addr + acc * kN + half * 128 + c * 32, r);
                         tmem_ld_wait();
-                        if (pr == 3) {
+                        if (c == 3) {
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(acc_empty + acc);
                         }
-                        const uint32_t* wp = sWp + pr * (64 / WPER);
-                        if constexpr (H == 128) {
-                            carry += head_sum_v41<64>(r, 0, wp, p.act);
-                            if (pr & 1) {
-                                store16(pr >> 1, carry);
-                                carry = 0.f;
+                        const uint32_t* wp = sWp + (half * 128 + c * 32) / WPER;
+                        if constexpr (H >= 32) {
+                            run += head_sum_v41<32>(r, 0, wp, p.act);
+                            if (((c + 1) * 32) % H == 0) {
+                                store16(half * QH + (c * 32) / H, run);
+                                run = 0.f;
                             }
                         } else {
 #pragma unroll
-                            for (int qq = 0; qq < 64 / H; ++qq)
-                                store16(pr * (64 / H) + qq, head_sum_v41<H>(r, qq * H, wp + (qq * H) / WPER, p.act));
+                            for (int qq = 0; qq < 32 / H; ++qq)
+                                store16(half * QH + c * (32 / H) + qq,
+                                        head_sum_v41<H>(r, qq * H, wp + (qq * H) / WPER, p.act));
                         }
                     }
                 }
@@ -484,9 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!computed) {
                     // tile outside every row's range: masked fill only
                     if (p.clean && t < p.Skv)
-                        for (int ql = 0; ql < QT; ++ql)
+                        for (int j = 0; j < QH; ++j) {
+                            const int ql = half * QH + j;
                             if (sHi[ql] >= 0)
                                 p.logits[((size_t)un.b * p.S + un.s0 + ql) * p.Skv + t] = ninf;
+                        }
                     continue;
                 }
                 const int acc = tcount & 1;
@@ -504,38 +542,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         rows[(size_t)ql * p.Skv_pad + t] = v;
                     }
                 };
-                float carry = 0.f;  // partial sum of a query spanning two column groups (H = 128)
+                // this warp's 128 columns as 4 chunks of 32
+                const float* wh = sW + half * 128;
+                float run = 0.f;  // partial sum of a query spanning several chunks
 #pragma unroll
-                for (int pr = 0; pr < 4; ++pr) {
-                    // columns [64*pr, 64*pr + 64) of the accumulator
-                    uint32_t r[64];
-                    tmem_ld32(lane_addr + acc * kN + pr * 64, *reinterpret_cast<uint32_t(*)[32]>(&r[0]));
-                    tmem_ld32(lane_addr + acc * kN + pr * 64 + 32,
-                              *reinterpret_cast<uint32_t(*)[32]>(&r[32]));
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(lane_addr + acc * kN + half * 128 + c * 32, r);
                     tmem_ld_wait();
-                    if (pr == 3) {
+                    if (c == 3) {
                         tc_fence_before();
                         __syncwarp();
                         if (lane == 0) mbar_arrive(acc_empty + acc);  // accumulator may be reused
                     }
-                    const float* wp = sW + pr * 64;
-                    if constexpr (H == 128) {
-                        carry += head_sum<64, 0>(r, wp, p.act);
-                        if (pr & 1) {
-                            store(pr >> 1, carry);
-                            carry = 0.f;
+                    if constexpr (H >= 32) {
+                        run += head_sum_at<32>(r, 0, wh + c * 32, p.act);
+                        if (((c + 1) * 32) % H == 0) {
+                            store(half * QH + (c * 32) / H, run);
+                            run = 0.f;
                         }
-                    } else if constexpr (H == 64) {
-                        store(pr, head_sum<64, 0>(r, wp, p.act));
-                    } else if constexpr (H == 32) {
-                        store(pr * 2, head_sum<32, 0>(r, wp, p.act));
-                        store(pr * 2 + 1, head_sum<32, 32>(r, wp + 32, p.act));
                     } else {
 #pragma unroll
-                        for (int qq = 0; qq < 64 / H; ++qq)
-                            store(pr * (64 / H) + qq,
-                                  head_sum<H, 0>(*reinterpret_cast<const uint32_t(*)[64]>(&r[qq * H]),
-                                                 wp + qq * H, p.act));
+                        for (int qq = 0; qq < 32 / H; ++qq)
+                            store(half * QH + c * (32 / H) + qq,
+                                  head_sum_at<H>(r, qq * H, wh + c * 32 + qq * H, p.act));
                     }
                 }
             }
@@ -548,7 +578,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ top-k
+        // two groups of four warps, each selecting its own rows of the tile
         const int ttid = threadIdx.x - 64 - kEpiThreads;
+        const int grp = ttid / kTopkGroupThreads, gtid = ttid % kTopkGroupThreads;
+        TopkSmem& sTg = *(TopkSmem*)(smem + L.topk_off + grp * ((sizeof(TopkSmem) + 15) / 16 * 16));
         int ucount = 0;
         bool ok = true;
         for (int i = 0; ok && select; ++i) {
@@ -561,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* rows = materialise
                                     ? nullptr
                                     : p.scratch + ((size_t)blockIdx.x * 2 + rb) * p.scratch_stride_cta;
-            for (int ql = 0; ql < QT; ++ql) {
+            for (int ql = grp; ql < QT; ql += kTopkGroups) {
                 const int s = un.s0 + ql;
                 if (s >= p.S) break;
                 int lo, hi;
@@ -569,8 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const size_t orow = ((size_t)un.b * p.S + s) * p.topk;
                 const float* row = materialise ? p.logits + ((size_t)un.b * p.S + s) * p.Skv
                                                : rows + (size_t)ql * p.Skv_pad;
-                row_topk<kTopkThreads>(row, lo, hi, p.topk, p.out_idx + orow, p.out_sc + orow, sT,
-                                       ttid, kTopkBar);
+                row_topk<kTopkGroupThreads>(row, lo, hi, p.topk, p.out_idx + orow, p.out_sc + orow, sTg,
+                                            gtid, kTopkBar + grp);
             }
             mbar_arrive(rows_empty + rb);
             ++ucount;
