@@ -8,8 +8,8 @@
 // index -1 / score -inf.
 //
 // Method (value-linear bucketing, exact):
-//   1. the row's visible scores are staged in shared memory (many loads in
-//      flight per thread), taking their min and max on the way.
+//   1. The row's visible scores are staged in shared memory (16-byte loads,
+//      all in flight at once), taking their min and max on the way.
 //   2. NB buckets linear in (max - v): bucket(v) = floor((max - v) * NB/(max-min)),
 //      clamped.  IEEE subtraction and multiplication are monotone, so a lower
 //      bucket always holds strictly larger scores than a higher one.
@@ -17,10 +17,10 @@
 //      the bucket holding the topk-th element is the threshold bucket.
 //   4. Members of buckets up to the threshold are scattered, grouped by
 //      bucket, into shared memory.
-//   5. Each member's final position is its bucket's start plus its rank among
-//      the bucket's members under (score desc, index asc); positions < topk
-//      are recorded in shared memory and written out coalesced.  Buckets are small for continuous scores; many exactly
-//      equal scores make a bucket large and that step quadratic in its size.
+//   5. Each candidate's position is its bucket's start plus its rank among the
+//      bucket's members under (score desc, index asc); positions < topk are
+//      recorded in shared memory and written out coalesced.  Many exactly equal
+//      scores make a bucket large and that step quadratic in its size.
 #pragma once
 #include <stdint.h>
 
@@ -31,9 +31,14 @@ namespace lidx {
 constexpr int kTopkBuckets = 2048;
 constexpr int kTopkCandMax = 4096;  // visible keys per row the selection supports
 
+// Histogram index of bucket b: one pad word per 32 buckets, so that lanes
+// reading runs of consecutive buckets hit distinct banks.
+__device__ __forceinline__ int hidx(int b) { return b + (b >> 5); }
+constexpr int kTopkHist = kTopkBuckets + kTopkBuckets / 32 + 1;
+
 struct TopkSmem {
     float row[kTopkCandMax];          // the row's visible scores, staged once
-    int start[kTopkBuckets + 1];      // bucket offsets; after the scatter, bucket ends
+    int start[kTopkHist];             // bucket offsets (padded); after the scatter, bucket ends
     uint16_t cand[kTopkCandMax];      // candidate keys (offsets into row), grouped by bucket
     uint16_t perm[kTopkCandMax];      // key at each output position
     float red_max[32];
@@ -44,7 +49,7 @@ struct TopkSmem {
 
 __device__ __forceinline__ int topk_bucket(float v, float vmax, float scale) {
     float x = __fmul_rn(__fsub_rn(vmax, v), scale);
-    int b = (int)x;  // x >= 0 and finite
+    int b = (int)x;  // x >= 0 (saturating conversion for huge x)
     return b < kTopkBuckets ? b : kTopkBuckets - 1;
 }
 
@@ -65,7 +70,31 @@ __device__ void row_topk(const float* row, int lo, int hi, int topk, int32_t* ou
     if (n > 0) {
         // 1. stage the row in shared memory; min / max on the way
         float vmax = ninf, vmin = __int_as_float(0x7f800000);
-        for (int base = 0; base < n; base += NT * UNR) {
+        int done = 0;
+        if ((((uintptr_t)(row + lo)) & 15) == 0) {
+            // aligned row: 16-byte loads, all of a thread's loads in flight at once
+            const int n4 = n / 4;
+            const float4* r4 = reinterpret_cast<const float4*>(row + lo);
+            for (int base = 0; base < n4; base += NT * UNR) {
+                float4 v[UNR];
+#pragma unroll
+                for (int k = 0; k < UNR; ++k) {
+                    const int j = base + k * NT + tid;
+                    v[k] = j < n4 ? r4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+                for (int k = 0; k < UNR; ++k) {
+                    const int j = base + k * NT + tid;
+                    if (j < n4) {
+                        reinterpret_cast<float4*>(sm.row)[j] = v[k];
+                        vmax = fmaxf(fmaxf(vmax, fmaxf(v[k].x, v[k].y)), fmaxf(v[k].z, v[k].w));
+                        vmin = fminf(fminf(vmin, fminf(v[k].x, v[k].y)), fminf(v[k].z, v[k].w));
+                    }
+                }
+            }
+            done = n4 * 4;
+        }
+        for (int base = done; base < n; base += NT * UNR) {
             float v[UNR];
 #pragma unroll
             for (int k = 0; k < UNR; ++k) {
@@ -91,7 +120,7 @@ __device__ void row_topk(const float* row, int lo, int hi, int topk, int32_t* ou
             sm.red_max[wid] = vmax;
             sm.red_min[wid] = vmin;
         }
-        for (int i = tid; i <= kTopkBuckets; i += NT) sm.start[i] = 0;
+        for (int i = tid; i < kTopkHist; i += NT) sm.start[i] = 0;
         named_bar_sync(bar_id, NT);
         vmax = sm.red_max[0];
         vmin = sm.red_min[0];
@@ -109,36 +138,36 @@ __device__ void row_topk(const float* row, int lo, int hi, int topk, int32_t* ou
             if (!(scale < __int_as_float(0x7f800000))) scale = 0.f;  // overflowed range
             // 2. histogram
 #pragma unroll 4
-            for (int j = tid; j < n; j += NT) atomicAdd(&sm.start[topk_bucket(sm.row[j], vmax, scale)], 1);
+            for (int j = tid; j < n; j += NT)
+                atomicAdd(&sm.start[hidx(topk_bucket(sm.row[j], vmax, scale))], 1);
             named_bar_sync(bar_id, NT);
-            // 3. exclusive scan.  Warp w owns buckets [w*SEG, (w+1)*SEG); lane l
-            //    reads buckets l, l+32, ... of it, so reads hit 32 distinct banks.
-            constexpr int SEG = kTopkBuckets / NW;
-            static_assert(kTopkBuckets % (NW * 32) == 0, "bucket split");
-            {
-                int wtotal = 0;
-#pragma unroll 4
-                for (int i = 0; i < SEG; i += 32) wtotal += sm.start[wid * SEG + i + lane];
+            // 3. exclusive scan: thread tid owns buckets [tid*PER, tid*PER + PER)
+            constexpr int PER = kTopkBuckets / NT;
+            static_assert(kTopkBuckets % NT == 0 && PER >= 1, "bucket split");
+            int cnt[PER];
+            int local = 0;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) wtotal += __shfl_xor_sync(0xffffffffu, wtotal, o);
-                if (lane == 0) sm.wsum[wid] = wtotal;
+            for (int i = 0; i < PER; ++i) {
+                cnt[i] = sm.start[hidx(tid * PER + i)];
+                local += cnt[i];
             }
-            named_bar_sync(bar_id, NT);
-            int carry = 0;
-            for (int i = 0; i < wid; ++i) carry += sm.wsum[i];
-            for (int i = 0; i < SEG; i += 32) {
-                const int b = wid * SEG + i + lane;
-                const int c = sm.start[b];
-                int incl = c;
+            int incl = local;
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                const int excl = carry + incl - c;
-                sm.start[b] = excl;
-                if (excl < sel && excl + c >= sel) sm.bstar = b;
-                carry += __shfl_sync(0xffffffffu, incl, 31);
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (lane == 31) sm.wsum[wid] = incl;
+            named_bar_sync(bar_id, NT);
+            int base = incl - local;
+#pragma unroll
+            for (int i = 0; i < NW; ++i) base += i < wid ? sm.wsum[i] : 0;
+#pragma unroll
+            for (int i = 0; i < PER; ++i) {
+                const int b = tid * PER + i;
+                sm.start[hidx(b)] = base;
+                if (base < sel && base + cnt[i] >= sel) sm.bstar = b;
+                base += cnt[i];
             }
             named_bar_sync(bar_id, NT);
             const int bstar = sm.bstar;
@@ -147,21 +176,27 @@ __device__ void row_topk(const float* row, int lo, int hi, int topk, int32_t* ou
 #pragma unroll 4
             for (int j = tid; j < n; j += NT) {
                 const int b = topk_bucket(sm.row[j], vmax, scale);
-                if (b <= bstar) sm.cand[atomicAdd(&sm.start[b], 1)] = (uint16_t)j;
+                if (b <= bstar) sm.cand[atomicAdd(&sm.start[hidx(b)], 1)] = (uint16_t)j;
             }
             named_bar_sync(bar_id, NT);
-            const int ncand = sm.start[bstar];
-            // 5. rank inside the bucket [end(b-1), end(b)); record the key at its position
+            // 5. rank each candidate inside its bucket [end(b-1), end(b));
+            //    record the key at its output position
+            const int ncand = sm.start[hidx(bstar)];
             for (int pidx = tid; pidx < ncand; pidx += NT) {
                 const int j = sm.cand[pidx];
                 const float v = sm.row[j];
                 const int b = topk_bucket(v, vmax, scale);
-                const int s0 = b == 0 ? 0 : sm.start[b - 1], e0 = sm.start[b];
+                const int s0 = b == 0 ? 0 : sm.start[hidx(b - 1)], e0 = sm.start[hidx(b)];
                 int rank = 0;
-                for (int qq = s0; qq < e0; ++qq) {
-                    const int jq = sm.cand[qq];
-                    const float vq = sm.row[jq];
-                    rank += (vq > v) || (vq == v && jq < j);
+                for (int qq = s0; qq < e0; qq += 4) {
+                    int jq[4];
+                    float vq[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) jq[u] = qq + u < e0 ? sm.cand[qq + u] : j;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) vq[u] = sm.row[jq[u]];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) rank += (vq[u] > v) || (vq[u] == v && jq[u] < j);
                 }
                 const int pos = s0 + rank;
                 if (pos < sel) sm.perm[pos] = (uint16_t)j;
