@@ -11,7 +11,9 @@
 //
 // One CTA per query row.  The row's queries stay in shared memory; its
 // selected keys are gathered in chunks of J.  Per chunk three small
-// contractions run on the CUDA cores with register tiles of four:
+// contractions run, on warp-level tf32 MMA tiles when H is a multiple of 16
+// (bwd_rows_mma_kernel) and on the CUDA cores with register tiles of four
+// otherwise (bwd_rows_kernel):
 //     X [H x J]  = Q [H x D] . Kc^T        (then dw and C = g*w*act'(x))
 //     dq[H x D] += C [H x J] . Kc [J x D]  (accumulated in registers)
 //     dKc[J x D] = C^T [J x H] . Q [H x D] (scatter-added to dk)
@@ -181,6 +183,193 @@ __global__ void __launch_bounds__(kBwdThreads)
     }
 }
 
+__device__ __forceinline__ uint32_t tf32_round(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
+}
+
+// d (16x8, fp32) += a (16x8, tf32, row) * b (8x8, tf32, col)
+__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Same computation as bwd_rows_kernel with the three contractions on warp-level
+// tf32 MMA tiles (m16n8k8).  q and k are exact in tf32 (bf16 values); the
+// accumulators are fp32; C = g*w*act'(x) is rounded to tf32 (nearest).  Fragment
+// coordinates: g = lane/4, c = lane%4; A rows g and g+8, columns c and c+4;
+// B column g, rows c and c+4; D rows g and g+8, columns 2c and 2c+1.
+template <int H>
+__global__ void __launch_bounds__(kBwdThreads)
+    bwd_rows_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                        const float* __restrict__ w, const int32_t* __restrict__ idx,
+                        const float* __restrict__ grad, int B, int S, int Skv, int D, int ratio,
+                        int topk, int act, float* __restrict__ dq, float* __restrict__ dk,
+                        float* __restrict__ dw) {
+    static_assert(H % 16 == 0, "H must be a multiple of 16");
+    extern __shared__ __align__(16) float sm[];
+    const int DP = D + 4;
+    constexpr int JP = kBwdJ + 4;
+    float* qs = sm;                      // [H][DP]
+    float* kc = qs + H * DP;             // [J][DP]
+    float* cs = kc + kBwdJ * DP;         // [H][JP]  C as tf32
+    float* ws = cs + H * JP;             // [H]
+    float* dws = ws + H;                 // [H]
+    float* gs = dws + H;                 // [J]
+    int* ts = reinterpret_cast<int*>(gs + kBwdJ);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, c4 = lane & 3;
+    constexpr int NWARP = kBwdThreads / 32;
+    constexpr int MT = H / 16;
+    const int NTD = D / 8;
+    constexpr int QT_MAX = (MT * 16 + NWARP - 1) / NWARP;  // dq tiles per warp at D = 128
+    auto u32 = [](float x) { return __float_as_uint(x); };
+
+    for (int r = blockIdx.x; r < B * S; r += gridDim.x) {
+        const int b = r / S, s = r % S;
+        const long long ke_ll = (long long)(s + 1) / ratio;
+        const int ke = (int)(ke_ll < Skv ? ke_ll : Skv);
+        __syncthreads();
+        for (int e = tid; e < H * D; e += kBwdThreads) {
+            const int h = e / D, d = e % D;
+            qs[h * DP + d] = bf16_to_f(q[(((size_t)s * B + b) * H + h) * D + d]);
+        }
+        for (int h = tid; h < H; h += kBwdThreads) {
+            ws[h] = w[((size_t)s * B + b) * H + h];
+            dws[h] = 0.f;
+        }
+        float accq[QT_MAX][4];
+#pragma unroll
+        for (int i = 0; i < QT_MAX; ++i)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accq[i][e] = 0.f;
+
+        const int32_t* irow = idx + (size_t)r * topk;
+        const float* grow = grad + (size_t)r * topk;
+        for (int j0 = 0; j0 < topk; j0 += kBwdJ) {
+            __syncthreads();
+            for (int j = tid; j < kBwdJ; j += kBwdThreads) {
+                const int slot = j0 + j;
+                int t = slot < topk ? irow[slot] : -1;
+                if (t < 0 || t >= ke) t = -1;
+                ts[j] = t;
+                gs[j] = t >= 0 ? grow[slot] : 0.f;
+            }
+            __syncthreads();
+            for (int e = tid; e < kBwdJ * D; e += kBwdThreads) {
+                const int j = e / D, d = e % D;
+                const int t = ts[j];
+                kc[j * DP + d] = t >= 0 ? bf16_to_f(k[((size_t)t * B + b) * D + d]) : 0.f;
+            }
+            __syncthreads();
+            // X = Q . Kc^T  [H x J]; then C and dw
+            for (int tt = warp; tt < MT * (kBwdJ / 8); tt += NWARP) {
+                const int mt = tt / (kBwdJ / 8), nt = tt % (kBwdJ / 8);
+                float x[4] = {0.f, 0.f, 0.f, 0.f};
+                const float* qa = qs + (mt * 16 + g) * DP + c4;
+                const float* kb = kc + (nt * 8 + g) * DP + c4;
+                for (int kk = 0; kk < D; kk += 8)
+                    mma_tf32(x, u32(qa[kk]), u32(qa[8 * DP + kk]), u32(qa[kk + 4]), u32(qa[8 * DP + kk + 4]),
+                             u32(kb[kk]), u32(kb[kk + 4]));
+                float dwp[2] = {0.f, 0.f};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = mt * 16 + g + (e >> 1) * 8, j = nt * 8 + 2 * c4 + (e & 1);
+                    const float xv = x[e], gv = gs[j];
+                    const float a = act == 0 ? fmaxf(xv, 0.f) : xv;
+                    const float da = act == 0 ? (xv > 0.f ? 1.f : 0.f) : 1.f;
+                    dwp[e >> 1] = fmaf(gv, a, dwp[e >> 1]);
+                    cs[h * JP + j] = __uint_as_float(tf32_round(gv * ws[h] * da));
+                }
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    dwp[u] += __shfl_xor_sync(0xffffffffu, dwp[u], 1);
+                    dwp[u] += __shfl_xor_sync(0xffffffffu, dwp[u], 2);
+                }
+                if (c4 == 0) {
+                    atomicAdd(&dws[mt * 16 + g], dwp[0]);
+                    atomicAdd(&dws[mt * 16 + g + 8], dwp[1]);
+                }
+            }
+            __syncthreads();
+            // dq += C . Kc  [H x D], tiles kept in registers across chunks
+#pragma unroll
+            for (int i = 0; i < QT_MAX; ++i) {
+                const int tt = warp + i * NWARP;
+                if (tt < MT * NTD) {
+                    const int mt = tt / NTD, nt = tt % NTD;
+                    const float* ca = cs + (mt * 16 + g) * JP + c4;
+                    const float* kb = kc + c4 * DP + nt * 8 + g;
+#pragma unroll
+                    for (int kk = 0; kk < kBwdJ; kk += 8)
+                        mma_tf32(accq[i], u32(ca[kk]), u32(ca[8 * JP + kk]), u32(ca[kk + 4]),
+                                 u32(ca[8 * JP + kk + 4]), u32(kb[kk * DP]), u32(kb[(kk + 4) * DP]));
+                }
+            }
+            // dKc = C^T . Q  [J x D], scatter-added to dk
+            for (int tt = warp; tt < (kBwdJ / 16) * NTD; tt += NWARP) {
+                const int mt = tt / NTD, nt = tt % NTD;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                const float* ca = cs + c4 * JP + mt * 16 + g;  // A[j][h] = C[h][j]
+                const float* qb = qs + c4 * DP + nt * 8 + g;
+#pragma unroll
+                for (int kk = 0; kk < H; kk += 8)
+                    mma_tf32(acc, u32(ca[kk * JP]), u32(ca[kk * JP + 8]), u32(ca[(kk + 4) * JP]),
+                             u32(ca[(kk + 4) * JP + 8]), u32(qb[kk * DP]), u32(qb[(kk + 4) * DP]));
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int j = mt * 16 + g + (e >> 1) * 8, d = nt * 8 + 2 * c4 + (e & 1);
+                    const int t = ts[j];
+                    if (t >= 0) atomicAdd(dk + ((size_t)t * B + b) * D + d, acc[e]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < QT_MAX; ++i) {
+            const int tt = warp + i * NWARP;
+            if (tt < MT * NTD) {
+                const int mt = tt / NTD, nt = tt % NTD;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int h = mt * 16 + g + (e >> 1) * 8, d = nt * 8 + 2 * c4 + (e & 1);
+                    dq[(((size_t)s * B + b) * H + h) * D + d] = accq[i][e];
+                }
+            }
+        }
+        __syncthreads();
+        for (int h = tid; h < H; h += kBwdThreads) dw[((size_t)s * B + b) * H + h] = dws[h];
+    }
+}
+
+static size_t bwd_mma_smem(int H, int D) {
+    const int DP = D + 4, JP = kBwdJ + 4;
+    return sizeof(float) * ((size_t)H * DP + (size_t)kBwdJ * DP + (size_t)H * JP + 2 * (size_t)H + kBwdJ) +
+           sizeof(int) * kBwdJ;
+}
+
+template <int H>
+static cudaError_t bwd_mma_h(const BwdLaunch& a) {
+    const size_t smem = bwd_mma_smem(H, a.D);
+    auto kern = bwd_rows_mma_kernel<H>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBwdThreads, smem);
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)a.num_sms * per_sm;
+    const int64_t rows = (int64_t)a.B * a.S;
+    if (grid > rows) grid = rows;
+    kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(
+        (const uint16_t*)a.q, (const uint16_t*)a.k, a.w, a.idx, a.grad, a.B, a.S, a.Skv, a.D, a.ratio,
+        a.topk, a.act, a.dq, a.dk, a.dw);
+    return cudaGetLastError();
+}
+
 static size_t bwd_smem(int H, int D) {
     const int DP = D + 4, JP = kBwdJ + 4;
     return sizeof(float) * ((size_t)H * DP + (size_t)kBwdJ * DP + (size_t)D * JP + (size_t)H * JP +
@@ -216,10 +405,10 @@ cudaError_t bwd_launch(const BwdLaunch& a) {
         case 2: return bwd_h<2>(a);
         case 4: return bwd_h<4>(a);
         case 8: return bwd_h<8>(a);
-        case 16: return bwd_h<16>(a);
-        case 32: return bwd_h<32>(a);
-        case 64: return bwd_h<64>(a);
-        case 128: return bwd_h<128>(a);
+        case 16: return bwd_mma_h<16>(a);
+        case 32: return bwd_mma_h<32>(a);
+        case 64: return bwd_mma_h<64>(a);
+        case 128: return bwd_mma_h<128>(a);
         default: return cudaErrorInvalidValue;
     }
 }
