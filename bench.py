@@ -299,7 +299,7 @@ def side_workloads(lidx, pk):
     fl = sel * 6.0 * wl.H * wl.D
     out["bwd"] = {"ms": ms, "selected_pairs": sel, "tflops": fl / ms / 1e9,
                   "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
-                  "kernel": "bwd_rows_kernel<64> (CUDA cores)", "launches": 2}
+                  "kernel": "bwd_rows_mma_kernel<64> (warp-level tf32 MMA)", "launches": 2}
     del q, k, w, idx, grad, outs
     return out
 
