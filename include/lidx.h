@@ -78,13 +78,15 @@ typedef enum { LIDX_OP_INDEXER_FWD = 0, LIDX_OP_INDEXER_BWD = 1, LIDX_OP_SCORES_
  *               logits are never written to HBM (fused path; needs workspace).
  *   topk_indices_in  int32 [B,S,topk], nullable.  Non-NULL: no selection; the
  *               scores of the given indices are returned (entries outside the
- *               row's visible range give -inf) and indices_out is a copy.
+ *               row's visible range give -inf), computed without a dense sweep
+ *               unless logits_out is also given, and indices_out is a copy.
  *   indices_out int32 [B,S,topk]  scores_out fp32 [B,S,topk]: sorted by score
  *               descending, equal scores by ascending index; rows with fewer
  *               than topk visible keys end with index -1 / score -inf.
  *   workspace   device scratch of lidx_workspace_bytes(LIDX_OP_INDEXER_FWD,..)
  *               bytes (may be NULL when that is 0), 256-byte aligned.
- *   Limits of this build: Skv <= 4096 when a selection is made.
+ *   Limits of this build: Skv <= 4096 when a selection is made (no limit with
+ *   topk_indices_in).
  */
 int lidx_indexer_fwd(const void* q, const void* k, const float* w,
                      int64_t B, int64_t S, int64_t Skv, int H, int D,

@@ -132,10 +132,44 @@ int lidx_indexer_fwd(const void* q, const void* k, const float* w, int64_t B, in
         return LIDX_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(w) || (logits_out && !aligned16(logits_out)))
         return LIDX_ERR_ALIGN;
-    if (topk_indices_in) return LIDX_ERR_UNSUPPORTED;
-    if (Skv > kTopkCandMax) return LIDX_ERR_UNSUPPORTED;
+    if (topk_indices_in && !aligned16(topk_indices_in)) return LIDX_ERR_ALIGN;
+    if (!topk_indices_in && Skv > kTopkCandMax) return LIDX_ERR_UNSUPPORTED;
     const int sms = device_sms(true);
     if (sms <= 0) return LIDX_ERR_NO_DEVICE;
+    if (topk_indices_in && Skv > 0) {
+        // given indices: no selection, score exactly those pairs
+        cudaStream_t st = (cudaStream_t)stream;
+        if (logits_out) {
+            // logits were asked for: sweep them, then gather (masked entries are -inf)
+            const int rc2 = lidx_indexer_logits(q, k, w, B, S, Skv, H, D, compress_ratio, nullptr,
+                                                nullptr, 1, act, logits_out, stream);
+            if (rc2) return rc2;
+            if (extract_launch(logits_out, topk_indices_in, B * S, Skv, topk, scores_out, st) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(indices_out, topk_indices_in, sizeof(int32_t) * (size_t)(B * S * topk),
+                                cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+                return LIDX_ERR_CUDA;
+            return LIDX_OK;
+        }
+        GatherLaunch g;
+        g.q = q;
+        g.k = k;
+        g.w = w;
+        g.idx = topk_indices_in;
+        g.B = (int)B;
+        g.S = (int)S;
+        g.Skv = (int)Skv;
+        g.H = H;
+        g.D = D;
+        g.ratio = compress_ratio;
+        g.topk = topk;
+        g.act = act;
+        g.out_idx = indices_out;
+        g.out_sc = scores_out;
+        g.stream = st;
+        g.num_sms = sms;
+        return gather_launch(g) == cudaSuccess ? LIDX_OK : LIDX_ERR_CUDA;
+    }
     if (Skv == 0)  // no keys at all: every row is padding, logits has no entries
         return pad_launch(B * S * (int64_t)topk, indices_out, scores_out, (cudaStream_t)stream) ==
                        cudaSuccess

@@ -183,22 +183,6 @@ __global__ void __launch_bounds__(kBwdThreads)
     }
 }
 
-__device__ __forceinline__ uint32_t tf32_round(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
-}
-
-// d (16x8, fp32) += a (16x8, tf32, row) * b (8x8, tf32, col)
-__device__ __forceinline__ void mma_tf32(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // Same computation as bwd_rows_kernel with the three contractions on warp-level
 // tf32 MMA tiles (m16n8k8).  q and k are exact in tf32 (bf16 values); the
 // accumulators are fp32; C = g*w*act'(x) is rounded to tf32 (nearest).  Fragment

@@ -74,6 +74,20 @@ struct BwdLaunch {
 };
 cudaError_t bwd_launch(const BwdLaunch& a);
 
+// forward with given indices (gather.cu)
+struct GatherLaunch {
+    const void* q;
+    const void* k;
+    const float* w;
+    const int32_t* idx;
+    int B, S, Skv, H, D, ratio, topk, act;
+    int32_t* out_idx;
+    float* out_sc;
+    cudaStream_t stream;
+    int num_sms;
+};
+cudaError_t gather_launch(const GatherLaunch& a);
+
 cudaError_t pad_launch(int64_t n, int32_t* idx, float* sc, cudaStream_t stream);
 
 // per-TU status readers (see LIDX_STATUS_READER): value, or -1 on a CUDA error

@@ -187,3 +187,31 @@ def test_long_context_fused_sampled_rows():
     q, k, w = workloads.v4_inputs(wl, 0)
     rows = workloads.sample_rows(wl.B, wl.S, 509, 3)
     full_check(q, k, w, wl.ratio, wl.topk, materialise=False, rows=rows)
+
+
+@pytest.mark.parametrize("H,D,B,S,Skv,ratio,topk", [
+    (64, 128, 1, 4096, 1024, 4, 512),   # c4-layer shapes, tensor-core path
+    (8, 32, 2, 300, 90, 4, 20),         # plain-FMA path
+    (128, 64, 1, 200, 6000, 1, 37),     # Skv beyond the selection limit is fine here
+])
+def test_given_indices_score_only_those_pairs(H, D, B, S, Skv, ratio, topk):
+    """topk_indices given: no selection; scores of exactly those pairs, -inf for
+    indices outside the row's causal range (padding -1 included)."""
+    g = np.random.default_rng(H + S)
+    q = workloads.to_bf16(g.standard_normal((S, B, H, D)).astype(np.float32) / np.sqrt(D))
+    k = workloads.to_bf16(g.standard_normal((Skv, B, D)).astype(np.float32) / np.sqrt(D))
+    w = torch.from_numpy((g.standard_normal((S, B, H)) / np.sqrt(H)).astype(np.float32))
+    ks, ke = oracle.causal_ranges(S, Skv, ratio)
+    idx = workloads.random_selection(B, S, Skv, topk, ke - ks, 2).numpy()
+    junk = g.random(idx.shape) < 0.05  # some indices past the range or negative
+    idx[junk] = g.integers(-3, Skv + 3, int(junk.sum()))
+    qd, kd, wd = cuda(q, k, w)
+    idd = torch.from_numpy(idx).to(DEV)
+    ref = oracle.gather_scores_rows(q, k, w, ks, ke, idx.reshape(B * S, topk))
+    for materialise in (False, True):
+        oi, osc, _ = lidx.lidx_indexer_fwd(qd, kd, wd, ratio, topk, topk_indices=idd,
+                                           materialise_logits=materialise)
+        torch.cuda.synchronize()
+        assert lidx.lidx_device_status() == 0
+        assert np.array_equal(oi.cpu().numpy(), idx)
+        assert_scores_close(osc.cpu().numpy().reshape(B * S, topk), ref, "given-index scores")
