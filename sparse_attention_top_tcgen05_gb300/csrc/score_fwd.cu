@@ -263,7 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                      const ScoreParams p) {
     constexpr int QT = kN / H;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    // 1024-byte aligned base, formed by pointer arithmetic on the shared array
+    // itself so that every access through it stays a shared-memory access
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const SmemLayout L = smem_layout(p.D);
     uint8_t* sQ = smem + L.q_off;
     uint8_t* sK = smem + L.k_off;
