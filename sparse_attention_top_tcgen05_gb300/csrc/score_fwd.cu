@@ -38,13 +38,13 @@ constexpr int kN = 256;            // UMMA N: query x head columns per tile
 constexpr int kM = 128;            // UMMA M: keys per tile
 constexpr int kStages = 2;         // key-tile ring depth
 constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, 128 columns each
-constexpr int kTopkWarps = 8;
+constexpr int kTopkWarps = 9;   // three selection groups of three warps
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kTopkThreads = 32 * kTopkWarps;
 constexpr int kThreads = 64 + kEpiThreads + kTopkThreads;
 constexpr int kEpiBar = 1;         // named barrier id of the epilogue group
-constexpr int kTopkBar = 2;        // named barrier ids of the two selection groups: 2, 3
-constexpr int kTopkGroups = 2;     // rows selected concurrently
+constexpr int kTopkBar = 2;        // named barrier ids of the selection groups: 2, 3, 4
+constexpr int kTopkGroups = 3;     // rows selected concurrently
 constexpr int kTopkGroupThreads = kTopkThreads / kTopkGroups;
 
 struct Unit {
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(acc_full + i, 1);
             mbar_init(acc_empty + i, kEpiWarps);
             mbar_init(rows_full + i, kEpiThreads);
-            mbar_init(rows_empty + i, kTopkThreads);
+            mbar_init(rows_empty + i, QT);  // one arrival per selected row
         }
         fence_mbar_init();
         tma_prefetch_desc(&tmq);
@@ -580,35 +580,47 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ top-k
-        // two groups of four warps, each selecting its own rows of the tile
+        // Group g selects rows g, g+G, g+2G, ... of this CTA's sequence of units
+        // (QT rows each), so the load spreads evenly whatever QT is.  A group
+        // waits for every unit's rows in turn, even one holding none of its
+        // rows, so that it never tests a row-slot barrier two phases behind.
         const int ttid = threadIdx.x - 64 - kEpiThreads;
         const int grp = ttid / kTopkGroupThreads, gtid = ttid % kTopkGroupThreads;
         TopkSmem& sTg = *(TopkSmem*)(smem + L.topk_off + grp * ((sizeof(TopkSmem) + 15) / 16 * 16));
-        int ucount = 0;
-        bool ok = true;
-        for (int i = 0; ok && select; ++i) {
-            const int u = unit_of(i, p.num_units);
-            if (u == -2) break;
-            if (u < 0) continue;
-            const Unit un = make_unit<QT, V41>(p, u);
-            const int rb = ucount & 1;
-            if (!(ok = mbar_wait(rows_full + rb, (ucount >> 1) & 1))) break;
-            const float* rows = materialise
-                                    ? nullptr
-                                    : p.scratch + ((size_t)blockIdx.x * 2 + rb) * p.scratch_stride_cta;
-            for (int ql = grp; ql < QT; ql += kTopkGroups) {
-                const int s = un.s0 + ql;
-                if (s >= p.S) break;
+        int i = 0, ucount = -1;
+        Unit un{};
+        bool ok = select;
+        for (int r = grp; ok; r += kTopkGroups) {
+            const int uc = r / QT, ql = r % QT;
+            bool more = true;
+            while (ok && ucount < uc) {
+                int u;
+                do {
+                    u = unit_of(i++, p.num_units);
+                } while (u == -1);
+                if (u == -2) {
+                    more = false;
+                    break;
+                }
+                un = make_unit<QT, V41>(p, u);
+                ++ucount;
+                ok = mbar_wait(rows_full + (ucount & 1), (ucount >> 1) & 1);
+            }
+            if (!more || !ok) break;
+            const int rb = uc & 1;
+            const int s = un.s0 + ql;
+            if (s < p.S) {
                 int lo, hi;
                 row_range(p, s, lo, hi);
                 const size_t orow = ((size_t)un.b * p.S + s) * p.topk;
-                const float* row = materialise ? p.logits + ((size_t)un.b * p.S + s) * p.Skv
-                                               : rows + (size_t)ql * p.Skv_pad;
+                const float* row = materialise
+                                       ? p.logits + ((size_t)un.b * p.S + s) * p.Skv
+                                       : p.scratch + ((size_t)blockIdx.x * 2 + rb) * p.scratch_stride_cta +
+                                             (size_t)ql * p.Skv_pad;
                 row_topk<kTopkGroupThreads>(row, lo, hi, p.topk, p.out_idx + orow, p.out_sc + orow, sTg,
-                                            gtid, kTopkBar + grp);
+                                            gtid, kTopkBar + grp);  // ends with a group barrier
             }
-            mbar_arrive(rows_empty + rb);
-            ++ucount;
+            if (gtid == 0) mbar_arrive(rows_empty + rb);  // this row's slot entry is free
         }
     }
 
