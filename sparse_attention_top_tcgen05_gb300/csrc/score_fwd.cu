@@ -38,7 +38,7 @@ constexpr int kN = 256;            // UMMA N: query x head columns per tile
 constexpr int kM = 128;            // UMMA M: keys per tile
 constexpr int kStages = 2;         // key-tile ring depth
 constexpr int kEpiWarps = 8;   // two per TMEM lane quadrant, 128 columns each
-constexpr int kTopkWarps = 12;  // three selection groups of four warps
+constexpr int kTopkWarps = 18;  // three selection groups of six warps
 constexpr int kEpiThreads = 32 * kEpiWarps;
 constexpr int kTopkThreads = 32 * kTopkWarps;
 constexpr int kThreads = 64 + kEpiThreads + kTopkThreads;
