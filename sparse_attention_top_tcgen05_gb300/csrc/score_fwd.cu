@@ -12,15 +12,15 @@
 //     so the head reduction sum_h w*act(x) is a per-thread loop over columns
 //     with no cross-lane traffic, and logits stores are 128 consecutive keys.
 //   * warp 0 lane 0: TMA producer.  The query tile [QT*H rows, D] stays resident
-//     for the whole key sweep; key tiles [128, D] stream through a 3-stage ring.
+//     for the whole key sweep; key tiles [128, D] stream through a 2-stage ring.
 //   * warp 1 lane 0: tcgen05.mma issuer into two 256-column fp32 accumulators
 //     (512 TMEM columns), so the MMA of tile i+1 overlaps the epilogue of tile i.
-//   * warps 2..5: epilogue, one warp per TMEM lane quadrant.  tcgen05.ld ->
-//     act -> weighted head sum in fp32 (packed f32x2 FMAs) -> mask -> store
-//     (logits) or stash in one of two per-CTA L2-resident row buffers.
-//   * warps 6..13: top-k of the previous query tile's rows (topk.cuh), reading
-//     the row buffer the epilogue is not writing, so selection overlaps the
-//     next tile's key sweep.
+//   * warps 2..9: epilogue, two warps per TMEM lane quadrant (128 columns each).
+//     tcgen05.ld -> act -> weighted head sum in fp32 -> mask -> store (logits)
+//     or stash in one of two per-CTA L2-resident row buffers.
+//   * warps 10..27: top-k in three groups of six warps (topk.cuh).  Group g
+//     takes rows g, g+3, ... of the CTA's query tiles from the row buffer the
+//     epilogue is not writing, so selection overlaps the next tile's key sweep.
 //   * Key tiles past the tile's last visible key are never loaded or multiplied.
 //     Query tiles are dealt to CTAs heaviest-first in a snake order; the next
 //     tile's queries are prefetched into L2 while the current one is swept.
