@@ -59,6 +59,60 @@ __global__ void __launch_bounds__(kMaskThreads)
     }
 }
 
+// Same pass for 16-byte aligned rows (Skv % 16 == 0, aligned bases): each lane
+// reads 16 flags of up to four rows at once, so a warp keeps 2 KB of `allowed`
+// in flight and covers four key tiles (8 lanes each) per step.
+__global__ void __launch_bounds__(kMaskThreads)
+    v41_mask_kernel16(const uint8_t* __restrict__ allowed, uint16_t* __restrict__ out,
+                      uint8_t* __restrict__ tilemap, int B, int S, int Skv, int QT, int qtiles,
+                      int ntk) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    constexpr int NW = kMaskThreads / 32;
+    const int units = B * qtiles;
+    const int nchunks = (ntk + 3) / 4;  // 512-key chunks
+    for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
+        const int b = unit / qtiles, qt = unit % qtiles, s0 = qt * QT;
+        const int rows = min(QT, S - s0);
+        for (int ch = warp; ch < nchunks; ch += NW) {
+            const int t0 = ch * 512 + lane * 16;
+            const bool in = t0 < Skv;  // Skv % 16 == 0: all 16 keys inside or none
+            const uint8_t* base = allowed + ((size_t)b * S + s0) * Skv + (in ? t0 : 0);
+            uint32_t acc = 0;
+            int r = 0;
+            for (; r + 4 <= rows; r += 4) {
+                uint4 v[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    v[u] = in ? *reinterpret_cast<const uint4*>(base + (size_t)(r + u) * Skv)
+                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) acc |= v[u].x | v[u].y | v[u].z | v[u].w;
+            }
+            for (; r < rows; ++r) {
+                const uint4 v = in ? *reinterpret_cast<const uint4*>(base + (size_t)r * Skv)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+                acc |= v.x | v.y | v.z | v.w;
+            }
+            // any visible pair in this lane's 128-key tile (lanes 8g .. 8g+7)
+            uint32_t any = acc != 0 ? 1u : 0u;
+            any |= __shfl_xor_sync(0xffffffffu, any, 1);
+            any |= __shfl_xor_sync(0xffffffffu, any, 2);
+            any |= __shfl_xor_sync(0xffffffffu, any, 4);
+            const int kt = ch * 4 + (lane >> 3);
+            if ((lane & 7) == 0 && kt < ntk) tilemap[(size_t)unit * ntk + kt] = any ? 1 : 0;
+            if (!any && in) {
+                const uint4 ninf = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+                uint16_t* o = out + ((size_t)b * S + s0) * Skv + t0;
+                for (int r2 = 0; r2 < rows; ++r2) {
+                    uint4* d = reinterpret_cast<uint4*>(o + (size_t)r2 * Skv);
+                    d[0] = ninf;
+                    d[1] = ninf;
+                }
+            }
+        }
+    }
+}
+
 cudaError_t v41_mask_launch(const uint8_t* allowed, uint16_t* out, uint8_t* tilemap, int B, int S,
                             int Skv, int QT, cudaStream_t stream) {
     const int qtiles = (S + QT - 1) / QT, ntk = (Skv + 127) / 128;
@@ -69,8 +123,12 @@ cudaError_t v41_mask_launch(const uint8_t* allowed, uint16_t* out, uint8_t* tile
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     int64_t grid = (int64_t)sms * 8;
     if (grid > units) grid = units;
-    v41_mask_kernel<<<(unsigned)grid, kMaskThreads, 0, stream>>>(allowed, out, tilemap, B, S, Skv, QT,
-                                                                 qtiles, ntk);
+    if ((Skv & 15) == 0 && ((((uintptr_t)allowed) | ((uintptr_t)out)) & 15) == 0)
+        v41_mask_kernel16<<<(unsigned)grid, kMaskThreads, 0, stream>>>(allowed, out, tilemap, B, S,
+                                                                       Skv, QT, qtiles, ntk);
+    else
+        v41_mask_kernel<<<(unsigned)grid, kMaskThreads, 0, stream>>>(allowed, out, tilemap, B, S, Skv,
+                                                                     QT, qtiles, ntk);
     return cudaGetLastError();
 }
 

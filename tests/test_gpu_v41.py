@@ -102,6 +102,11 @@ def test_packed_documents_full_size_sampled():
     (2, 77, 1000, 16, 64, 0.05),
     (1, 64, 130, 1, 16, 0.9),
     (3, 40, 64, 32, 32, 1.0),
+    # Skv % 16 == 0 takes the 16-byte visibility pass: a ragged last key tile, a key-tile
+    # count that is not a multiple of four, blocks with no visible pair, none visible at all
+    (2, 100, 400, 8, 64, 0.3),
+    (1, 70, 208, 16, 32, 0.0005),
+    (1, 33, 272, 4, 16, 0.0),
 ])
 def test_shapes_random_visibility(B, S, Skv, H, D, density):
     g = np.random.default_rng(S + Skv)
