@@ -305,11 +305,19 @@ __global__ void __launch_bounds__(kBwdThreads)
                 for (int kk = 0; kk < H; kk += 8)
                     mma_tf32(acc, u32(ca[kk * JP]), u32(ca[kk * JP + 8]), u32(ca[(kk + 4) * JP]),
                              u32(ca[(kk + 4) * JP + 8]), u32(qb[kk * DP]), u32(qb[(kk + 4) * DP]));
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int j = mt * 16 + g + (e >> 1) * 8, d = nt * 8 + 2 * c4 + (e & 1);
-                    const int t = ts[j];
-                    if (t >= 0) atomicAdd(dk + ((size_t)t * B + b) * D + d, acc[e]);
+                // Lanes c4 and c4^1 swap halves so that each holds four consecutive d of
+                // one key (even c4: key row g, odd c4: key row g + 8), then one 16-byte
+                // vector reduction per lane instead of four scalar ones.
+                const bool odd = (c4 & 1) != 0;
+                const float s0 = __shfl_xor_sync(0xffffffffu, odd ? acc[0] : acc[2], 1);
+                const float s1 = __shfl_xor_sync(0xffffffffu, odd ? acc[1] : acc[3], 1);
+                const int j = mt * 16 + g + (odd ? 8 : 0);
+                const int d0 = nt * 8 + 2 * (c4 & 2);
+                const int t = ts[j];
+                if (t >= 0) {
+                    const float4 v = odd ? make_float4(s0, s1, acc[2], acc[3])
+                                         : make_float4(acc[0], acc[1], s0, s1);
+                    atomicAdd(reinterpret_cast<float4*>(dk + ((size_t)t * B + b) * D + d0), v);
                 }
             }
         }
