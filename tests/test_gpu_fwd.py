@@ -119,6 +119,8 @@ def test_c4_layer_workload_full():
     (32, 64, 3, 129, 40, 2, 50),         # topk > visible keys on every row
     (1, 16, 1, 513, 256, 2, 17),
     (2, 48, 2, 260, 70, 4, 5),
+    (128, 64, 2, 1000, 300, 2, 40),     # two rows per query tile, several tiles per CTA:
+                                         # some selection groups own no row of a tile
 ])
 def test_shapes_fused_and_materialised(H, D, B, S, Skv, ratio, topk):
     g = np.random.default_rng(H * 7 + D)
