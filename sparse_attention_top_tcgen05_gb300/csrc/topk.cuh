@@ -107,7 +107,7 @@ __device__ void row_topk(const float* row, int lo, int hi, int topk, int32_t* ou
                          float* out_sc, TopkSmem& sm, int tid, int bar_id) {
     static_assert(NT % 32 == 0 && NT <= 1024, "group size");
     constexpr int NW = NT / 32;
-    constexpr int UNR = 8;  // 16-byte loads in flight per thread in each pass over the row
+    constexpr int UNR = 4;  // 16-byte loads in flight per thread in each pass over the row
     const int lane = tid & 31, wid = tid >> 5;
     const int n = hi > lo ? hi - lo : 0;
     const int sel = n < topk ? n : topk;
