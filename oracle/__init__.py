@@ -56,6 +56,7 @@ def lib():
             L.orc_logits_rows.argtypes = [P, P, P, i64, i64, i64, i32, i32, P, P, i32, P, i64, P]
             L.orc_topk_rows.argtypes = [P, i64, i64, P, i64, P, P, i32, P, P]
             L.orc_extract_rows.argtypes = [P, i64, i64, P, i32, P]
+            L.orc_topk_masked_rows.argtypes = [P, P, i64, i64, i32, P, P]
             L.orc_gather_scores_rows.argtypes = [P, P, P, i64, i64, i64, i32, i32, P, P, i32,
                                                  P, i64, P, i32, P]
             L.orc_scores_v41_rows.argtypes = [P, P, P, P, i64, i64, i64, i32, i32, i32, P, i64, P]
@@ -129,6 +130,19 @@ def topk_rows(logits, S, ks, ke, topk, rows):
     idx = np.empty((nrows, topk), np.int32)
     sc = np.empty((nrows, topk), np.float64)
     rc = lib().orc_topk_rows(_p(lg), nrows, Skv, _p(r), S, _p(ksa), _p(kea), topk, _p(idx), _p(sc))
+    assert rc == 0
+    return idx, sc
+
+
+def topk_masked_rows(logits, mask, topk):
+    """Top-k of each row of ``logits`` [nrows, Skv] over the entries where
+    ``mask`` [nrows, Skv] is nonzero; padding -1 / -inf."""
+    lg = _np(logits, np.float64)
+    nrows, Skv = lg.shape
+    m = _np(mask, np.uint8).reshape(nrows, Skv)
+    idx = np.empty((nrows, topk), np.int32)
+    sc = np.empty((nrows, topk), np.float64)
+    rc = lib().orc_topk_masked_rows(_p(lg), _p(m), nrows, Skv, topk, _p(idx), _p(sc))
     assert rc == 0
     return idx, sc
 

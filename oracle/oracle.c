@@ -244,6 +244,61 @@ int orc_topk_rows(const double* logits, int64_t nrows, int64_t Skv,
     return 0;
 }
 
+/* Top-k over the entries of each row whose mask byte is nonzero ("deepseek_v41.
+ * indexer" page, module docstring: the top-k / candidate selection runs on the
+ * scorer's output over the visible keys).  Same order and padding as
+ * orc_topk_rows. */
+typedef struct {
+    const double* logits;
+    const uint8_t* mask;
+    int64_t Skv;
+    int topk;
+    int32_t* idx;
+    double* score;
+    cand** scratch;
+} topk_masked_ctx;
+
+static void topk_masked_row(void* p, int64_t i, int tid) {
+    topk_masked_ctx* c = (topk_masked_ctx*)p;
+    cand* buf = c->scratch[tid];
+    int64_t n = 0;
+    for (int64_t t = 0; t < c->Skv; ++t) {
+        if (!c->mask[i * c->Skv + t]) continue;
+        buf[n].v = c->logits[i * c->Skv + t];
+        buf[n].t = (int32_t)t;
+        ++n;
+    }
+    qsort(buf, (size_t)n, sizeof(cand), cand_cmp);
+    for (int j = 0; j < c->topk; ++j) {
+        if (j < n) {
+            c->idx[i * c->topk + j] = buf[j].t;
+            c->score[i * c->topk + j] = buf[j].v;
+        } else {
+            c->idx[i * c->topk + j] = -1;
+            c->score[i * c->topk + j] = -INFINITY;
+        }
+    }
+}
+
+int orc_topk_masked_rows(const double* logits, const uint8_t* mask, int64_t nrows, int64_t Skv,
+                         int topk, int32_t* idx_out, double* score_out) {
+    if (topk < 0) return 1;
+    int nt = orc_get_threads();
+    if (nt > 512) nt = 512;
+    cand* scratch[512];
+    for (int t = 0; t < nt; ++t) {
+        scratch[t] = (cand*)malloc(sizeof(cand) * (size_t)(Skv > 0 ? Skv : 1));
+        if (!scratch[t]) {
+            for (int u = 0; u < t; ++u) free(scratch[u]);
+            return 2;
+        }
+    }
+    topk_masked_ctx c = {logits, mask, Skv, topk, idx_out, score_out, scratch};
+    parallel_rows(nrows, topk_masked_row, &c, nt);
+    for (int t = 0; t < nt; ++t) free(scratch[t]);
+    return 0;
+}
+
 /* ------------------------------------------------------------------ extract */
 void orc_extract_rows(const double* logits, int64_t nrows, int64_t Skv,
                       const int32_t* idx, int topk, double* out) {

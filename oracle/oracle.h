@@ -49,6 +49,12 @@ int orc_topk_rows(const double* logits, int64_t nrows, int64_t Skv,
                   const int64_t* rows, int64_t S, const int32_t* ks, const int32_t* ke,
                   int topk, int32_t* idx_out, double* score_out);
 
+/* Per-row top-k over the entries whose mask byte is nonzero (the V4.1
+ * selection over visible keys): same order and padding as orc_topk_rows.
+ * logits and mask are [nrows, Skv]. */
+int orc_topk_masked_rows(const double* logits, const uint8_t* mask, int64_t nrows, int64_t Skv,
+                         int topk, int32_t* idx_out, double* score_out);
+
 /* pytorch_extract_topk_scores: out[i,j] = logits[i, idx[i,j]], -inf for an
  * index outside [0, Skv). */
 void orc_extract_rows(const double* logits, int64_t nrows, int64_t Skv,

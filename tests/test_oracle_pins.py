@@ -403,3 +403,76 @@ def test_bwd_identity_closed_form():
             sel = idx[b, s] >= 0
             gk = (grad[b, s, sel][:, None] * kf[idx[b, s, sel], b, :]).sum(0)
             np.testing.assert_allclose(dq[s, b], w.numpy()[s, b][:, None] * gk, rtol=1e-10, atol=1e-12)
+
+
+# ------------------------------------------------------------ masked top-k
+def test_topk_masked_matches_library_sort():
+    """Selection over arbitrary visible sets: numpy lexsort over the visible
+    entries of each row (ties included), padding past the visible count."""
+    g = np.random.default_rng(12)
+    n, Skv, topk = 40, 70, 24
+    lg = g.integers(-4, 5, (n, Skv)).astype(np.float64) * 0.5  # many exact ties
+    mask = (g.random((n, Skv)) < np.linspace(0.05, 0.9, n)[:, None]).astype(np.uint8)
+    idx, sc = oracle.topk_masked_rows(lg, mask, topk)
+    for i in range(n):
+        t = np.flatnonzero(mask[i])
+        order = np.lexsort((t, -lg[i, t]))
+        sel = t[order][:topk]
+        assert (idx[i, :sel.size] == sel).all() and (idx[i, sel.size:] == -1).all()
+        assert (sc[i, :sel.size] == lg[i, sel]).all() and np.isneginf(sc[i, sel.size:]).all()
+
+
+def test_topk_masked_contiguous_mask_equals_range_topk():
+    wl = workloads.WORKLOADS["tiny"]
+    q, k, w = workloads.v4_inputs(wl, 1)
+    ks, ke = oracle.causal_ranges(wl.S, wl.Skv, wl.ratio)
+    idx, sc, lg = oracle.indexer_fwd_rows(q, k, w, wl.ratio, wl.topk)
+    mask = (np.arange(wl.Skv)[None, :] < ke[:, None]).astype(np.uint8)
+    midx, msc = oracle.topk_masked_rows(np.nan_to_num(lg, neginf=0.0), mask, wl.topk)
+    assert np.array_equal(midx, idx) and np.array_equal(msc, sc)
+
+
+# ------------------------------------------------------ backward slack outputs
+def _slack_case(act):
+    """One row (s = 7, ratio 1) selecting key 0 with q.k = 0 exactly and key 1
+    with q.k = 3; H = 1, D = 16, w = 0.75, grads 0.5 and 2."""
+    S, Skv, D = 8, 2, 16
+    q = np.zeros((S, 1, 1, D), np.float32)
+    k = np.zeros((Skv, 1, D), np.float32)
+    q[7, 0, 0, :2] = [1, 1]
+    k[0, 0, :2] = [1, -1]
+    k[1, 0, :2] = [2, 1]
+    w = torch.full((S, 1, 1), 0.75)
+    idx = np.full((1, S, 2), -1, np.int32)
+    idx[0, 7] = [0, 1]
+    grad = np.zeros((1, S, 2), np.float32)
+    grad[0, 7] = [0.5, 2.0]
+    ks, ke = oracle.causal_ranges(S, Skv, 1)
+    return oracle.bwd(bf16(q), bf16(k), w, idx, grad, ks, ke, act=act), D
+
+
+def test_bwd_slack_marks_exactly_the_ambiguous_relu_pair():
+    (dq, dk, dw, sq, sk, sw), D = _slack_case("relu")
+    gamma = D * 2.0 ** -22
+    # ReLU'(0) = 0: only key 1 reaches dq and dk; dw = 0.5*relu(0) + 2*3
+    assert np.array_equal(dq[7, 0, 0, :3], [3.0, 1.5, 0.0]) and dw[7, 0, 0] == 6.0
+    assert np.array_equal(dk[0, 0, :3], [0, 0, 0]) and np.array_equal(dk[1, 0, :3], [1.5, 1.5, 0])
+    # the x = 0 pair widens the bound by |g w| |k| on dq, |g w| |q| on dk, |g| gamma sum|q k| on dw
+    assert np.array_equal(sq[7, 0, 0, :3], [0.375, 0.375, 0.0])
+    assert np.array_equal(sk[0, 0, :3], [0.375, 0.375, 0.0]) and (sk[1] == 0).all()
+    assert sw[7, 0, 0] == 0.5 * gamma * 2.0
+    sq[7, 0, 0, :2] = 0
+    sk[0, 0, :2] = 0
+    sw[7, 0, 0] = 0
+    assert not sq.any() and not sk.any() and not sw.any()
+
+
+def test_bwd_slack_is_zero_for_identity_and_far_from_kinks():
+    (dq, dk, dw, sq, sk, sw), _ = _slack_case("identity")
+    assert not sq.any() and not sk.any() and not sw.any()
+    assert np.array_equal(dq[7, 0, 0, :3], [0.75 * (0.5 * 1 + 2 * 2), 0.75 * (0.5 * -1 + 2 * 1), 0])
+    # all-positive queries and keys: every |x| is far above gamma * sum|q k|
+    q, k, w, idx, grad, ks, ke = _bwd_case(seed=6)
+    q, k = bf16(np.abs(f32(q)) + 0.5), bf16(np.abs(f32(k)) + 0.5)
+    *_, sq, sk, sw = oracle.bwd(q, k, w, idx, grad, ks, ke)
+    assert not sq.any() and not sk.any() and not sw.any()
