@@ -211,8 +211,17 @@ def run_reference(args, wl, world, rank):
 METRIC = "indexer valid-pair TFLOP/s and query-rows/s incl. top-k; % of GB300 BF16 peak"
 
 
+WORKLOAD_DESC = {
+    "tiny": "V4 score+causal mask+top-k, logits materialised",
+    "c4_fwd": "V4 C4-layer score+causal mask, logits materialised, then top-k",
+    "long_fused": "V4 fused score+causal mask+top-k, logits not materialised",
+    "bwd": "V4 fused score+causal mask+top-k at the backward workload's shape",
+}
+
+
 def config_of(wl, n):
-    return {"workload": f"{wl.name}: V4 fused score+causal mask+top-k, logits not materialised",
+    desc = WORKLOAD_DESC.get(wl.name, "V4 fused score+causal mask+top-k")
+    return {"workload": f"{wl.name}: {desc}",
             "B": wl.B, "S": wl.S, "H": wl.H, "D": wl.D, "Skv": wl.Skv,
             "compress_ratio": wl.ratio, "topk": wl.topk, "act": "relu",
             "inputs": "bf16 q,k ~N(0,1/D); fp32 w ~N(0,1/H); seed 0",
@@ -233,11 +242,60 @@ def time_steps(fn, steps, stream):
     return start.elapsed_time(end) / steps
 
 
+def _median_ms(fn, stream, reps, flush=None):
+    ts = []
+    for _ in range(reps):
+        if flush is not None:
+            flush.zero_()
+        ts.append(time_steps(fn, 1, stream))
+    return statistics.median(ts)
+
+
+def selection_rows(kind, rows, Skv, seed=0):
+    """Adversarial score rows for the selection timing (fp32 [rows, Skv])."""
+    g = np.random.default_rng(seed)
+    if kind == "normal":
+        x = g.standard_normal((rows, Skv))
+    elif kind == "ties":        # seven distinct values
+        x = g.integers(-3, 4, (rows, Skv)) * 0.5
+    elif kind == "const":
+        x = np.full((rows, Skv), 2.5)
+    elif kind == "zero_pad":    # most keys score exactly 0
+        x = g.standard_normal((rows, Skv))
+        x[:, Skv // 8:] = 0.0
+    elif kind == "two_values":
+        x = np.where(g.random((rows, Skv)) < 0.5, 1.0, -2.0)
+    else:
+        raise ValueError(kind)
+    return torch.from_numpy(x.astype(np.float32))
+
+
 def side_workloads(lidx, pk):
     """Short measurements of the other workloads' kernels (not the headline)."""
     out = {}
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    # tiny workload: latency of one call (logits materialised, then top-k)
+    wl = workloads.WORKLOADS["tiny"]
+    q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
+    idx = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.int32, device="cuda")
+    sc = torch.empty_like(idx, dtype=torch.float32)
+    lg = torch.empty(wl.B, wl.S, wl.Skv, dtype=torch.float32, device="cuda")
+    fn = lambda: lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk, materialise_logits=True,
+                                       out=(idx, sc, lg))
+    for _ in range(10):
+        fn()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(200):
+        fn()
+    torch.cuda.synchronize()
+    host_us = (time.perf_counter() - t0) / 200 * 1e6
+    out["tiny"] = {"us_per_call": 1e3 * time_steps(fn, 200, stream), "host_us_per_call": host_us,
+                   "launches": 1, "note": "back-to-back calls, L2 warm; host_us includes the "
+                   "Python binding and the C ABI's argument checks"}
+    del q, k, w, idx, sc, lg
 
     wl = workloads.WORKLOADS["c4_fwd"]
     q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
@@ -248,11 +306,7 @@ def side_workloads(lidx, pk):
                                        out=(idx, sc, lg))
     for _ in range(3):
         fn()
-    ts = []
-    for _ in range(10):
-        flush.zero_()
-        ts.append(time_steps(fn, 1, stream))
-    ms = statistics.median(ts)
+    ms = _median_ms(fn, stream, 10, flush)
     pairs = visible_pairs(wl.S, wl.Skv, wl.ratio, wl.B)
     fl = pairs * 2.0 * wl.H * wl.D
     alg_bytes = q.numel() * 2 + k.numel() * 2 + w.numel() * 4 + lg.numel() * 4 + idx.numel() * 8
@@ -260,7 +314,20 @@ def side_workloads(lidx, pk):
                      "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
                      "hbm_gbs": alg_bytes / ms / 1e6, "hbm_frac": alg_bytes / ms / 1e6 / pk["hbm_gbs"],
                      "l2": "256 MB flush before each launch"}
-    del q, k, w, idx, sc, lg
+    # the same layer with the previous selection given (no selection; scores of those keys)
+    given = idx.clone()
+    ws = torch.empty(lidx.lidx_workspace_bytes(lidx.OP_INDEXER_FWD, wl.B, wl.S, wl.Skv, wl.H, wl.D,
+                                               wl.topk), dtype=torch.uint8, device="cuda")
+    fn = lambda: lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk, topk_indices=given,
+                                       out=(idx, sc, None), workspace=ws)
+    for _ in range(3):
+        fn()
+    ms = _median_ms(fn, stream, 10, flush)
+    out["c4_fwd_given_indices"] = {"ms": ms, "tflops": fl / ms / 1e9,
+                                   "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
+                                   "note": "topk_indices given: same tensor-core sweep, the "
+                                   "selection replaced by a gather", "l2": "256 MB flush"}
+    del q, k, w, idx, sc, lg, given, ws
 
     # V4.1 packed documents: HBM-bound (q, allowed read; bf16 scores written)
     wl = workloads.WORKLOADS["v41_packed"]
@@ -271,11 +338,7 @@ def side_workloads(lidx, pk):
     fn = lambda: lidx.lidx_indexer_scores_v41(q, k, w, allowed, out=out16, workspace=ws)
     for _ in range(3):
         fn()
-    ts = []
-    for _ in range(10):
-        flush.zero_()
-        ts.append(time_steps(fn, 1, stream))
-    ms = statistics.median(ts)
+    ms = _median_ms(fn, stream, 10, flush)
     vis = int(allowed.sum().item())
     alg_bytes = (q.numel() * 2 + k.numel() * 2 + w.numel() * 2 + allowed.numel() + out16.numel() * 2)
     out["v41_packed"] = {"ms": ms, "hbm_gbs": alg_bytes / ms / 1e6,
@@ -283,7 +346,35 @@ def side_workloads(lidx, pk):
                          "algorithmic_bytes": alg_bytes, "visible_pairs": vis,
                          "visible_pair_tflops": vis * 2.0 * wl.H * wl.D / ms / 1e9,
                          "launches": 2, "l2": "256 MB flush before each call"}
-    del q, k, w, allowed, out16, ws
+    tidx = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.int32, device="cuda")
+    tsc = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.bfloat16, device="cuda")
+    wsb = lidx.lidx_workspace_bytes(lidx.OP_TOPK_V41, wl.B, wl.S, wl.Skv, wl.H, wl.D, wl.topk, True)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    fn = lambda: lidx.lidx_indexer_topk_v41(q, k, w, allowed, wl.topk, out=(out16, tidx, tsc),
+                                            workspace=ws)
+    for _ in range(3):
+        fn()
+    ms2 = _median_ms(fn, stream, 10, flush)
+    out["v41_packed_topk"] = {"ms": ms2, "topk": wl.topk, "selection_ms": ms2 - ms,
+                              "rows_per_s": wl.B * wl.S / ms2 * 1e3, "launches": 3,
+                              "l2": "256 MB flush before each call"}
+    del q, k, w, allowed, out16, ws, tidx, tsc
+
+    # selection alone on adversarial rows: time of a tie-heavy row against a normal one
+    rows, Skv, topk = 4096, 4096, 2048
+    sel = {}
+    for kind in ("normal", "ties", "const", "zero_pad", "two_values"):
+        x = selection_rows(kind, rows, Skv).cuda()
+        oi = torch.empty(rows, topk, dtype=torch.int32, device="cuda")
+        os_ = torch.empty(rows, topk, dtype=torch.float32, device="cuda")
+        fn = lambda: lidx.lidx_topk_rows(x, topk, out=(oi, os_))
+        for _ in range(3):
+            fn()
+        sel[kind] = time_steps(fn, 10, stream)
+        del x, oi, os_
+    out["selection"] = {"rows": rows, "Skv": Skv, "topk": topk, "ms": sel,
+                        "worst_over_normal": max(sel.values()) / sel["normal"],
+                        "kernel": "topk_rows_kernel (standalone selection, 256 threads per row)"}
 
     # backward through the selected entries (selection: the forward's own top-k)
     wl = workloads.WORKLOADS["bwd"]
@@ -292,17 +383,21 @@ def side_workloads(lidx, pk):
     grad = workloads.grad_scores(wl.B, wl.S, wl.topk, 0).cuda()
     outs = (torch.empty(wl.S, wl.B, wl.H, wl.D, device="cuda"), torch.empty(wl.Skv, wl.B, wl.D, device="cuda"),
             torch.empty(wl.S, wl.B, wl.H, device="cuda"))
-    fn = lambda: lidx.lidx_indexer_bwd(q, k, w, idx, grad, wl.ratio, out=outs)
+    wsb = lidx.lidx_workspace_bytes(lidx.OP_INDEXER_BWD, wl.B, wl.S, wl.Skv, wl.H, wl.D, wl.topk)
+    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+    fn = lambda: lidx.lidx_indexer_bwd(q, k, w, idx, grad, wl.ratio, out=outs, workspace=ws)
     for _ in range(2):
         fn()
     ms = time_steps(fn, 3, stream)
-    sel = int((idx >= 0).sum().item())
-    fl = sel * 6.0 * wl.H * wl.D
-    out["bwd"] = {"ms": ms, "selected_pairs": sel, "tflops": fl / ms / 1e9,
-                  "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
-                  "kernel": "bwd_rows_mma_kernel<64> (warp-level tf32 MMA)", "launches": 2}
-    del q, k, w, idx, grad, outs
+    nsel = int((idx >= 0).sum().item())
+    fl = nsel * 6.0 * wl.H * wl.D
+    out["bwd"] = {"ms": ms, "selected_pairs": nsel, "tflops": fl / ms / 1e9,
+                  "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"], "kernel": BWD_KERNEL}
+    del q, k, w, idx, grad, outs, ws
     return out
+
+
+BWD_KERNEL = "bwd_rows_mma_kernel<64> (warp-level tf32 MMA)"
 
 
 def run_gpu(args, wl, world, rank, local):

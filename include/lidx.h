@@ -66,7 +66,12 @@ typedef enum {
 typedef enum { LIDX_ACT_RELU = 0, LIDX_ACT_IDENTITY = 1 } lidx_act;
 
 /* Operation ids for lidx_workspace_bytes. */
-typedef enum { LIDX_OP_INDEXER_FWD = 0, LIDX_OP_INDEXER_BWD = 1, LIDX_OP_SCORES_V41 = 2 } lidx_op;
+typedef enum {
+    LIDX_OP_INDEXER_FWD = 0,
+    LIDX_OP_INDEXER_BWD = 1,
+    LIDX_OP_SCORES_V41 = 2,
+    LIDX_OP_TOPK_V41 = 3
+} lidx_op;
 
 /*
  * V4 forward: causal mask + per-row top-k   [P1 V4IndexerFunction.forward,
@@ -78,14 +83,15 @@ typedef enum { LIDX_OP_INDEXER_FWD = 0, LIDX_OP_INDEXER_BWD = 1, LIDX_OP_SCORES_
  *               logits are never written to HBM (fused path; needs workspace).
  *   topk_indices_in  int32 [B,S,topk], nullable.  Non-NULL: no selection; the
  *               scores of the given indices are returned (entries outside the
- *               row's visible range give -inf), computed without a dense sweep
- *               unless logits_out is also given, and indices_out is a copy.
+ *               row's visible range give -inf) and indices_out is a copy.  The
+ *               scores come from the same tensor-core sweep of the row's
+ *               visible keys (needs the workspace unless logits_out is given).
  *   indices_out int32 [B,S,topk]  scores_out fp32 [B,S,topk]: sorted by score
  *               descending, equal scores by ascending index; rows with fewer
  *               than topk visible keys end with index -1 / score -inf.
  *   workspace   device scratch of lidx_workspace_bytes(LIDX_OP_INDEXER_FWD,..)
  *               bytes (may be NULL when that is 0), 256-byte aligned.
- *   Limits of this build: Skv <= 4096 when a selection is made (no limit with
+ *   Limit of this build: Skv <= 65536 when a selection is made (no limit with
  *   topk_indices_in).
  */
 int lidx_indexer_fwd(const void* q, const void* k, const float* w,
@@ -94,6 +100,23 @@ int lidx_indexer_fwd(const void* q, const void* k, const float* w,
                      const int32_t* topk_indices_in, float* logits_out,
                      int32_t* indices_out, float* scores_out,
                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * V4 forward over explicit per-row ranges   [P2 batched_indexer_fwd /
+ * indexer_fwd_interface: cu_seqlen_ks, cu_seqlen_ke; P1 forward].  As
+ * lidx_indexer_fwd, except that row (b,s) sees keys t in
+ * [max(ks[s],0), min(ke[s],Skv)) instead of the causal range.  ks, ke: int32
+ * [S] device arrays, both required.  A context-parallel rank holding query
+ * rows [p0, p0+S) of a longer sequence, with every compressed key gathered
+ * [P3 indexer_scores, keys], passes ks = 0 and ke = min((p0+s+1)/compress_ratio,
+ * Skv) and gets exactly the rows of the unsharded call.
+ */
+int lidx_indexer_fwd_ranges(const void* q, const void* k, const float* w,
+                            int64_t B, int64_t S, int64_t Skv, int H, int D,
+                            const int32_t* ks, const int32_t* ke, int topk, int act,
+                            const int32_t* topk_indices_in, float* logits_out,
+                            int32_t* indices_out, float* scores_out,
+                            void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * The fused forward of lidx_indexer_fwd (logits not written, selection made)
@@ -149,7 +172,7 @@ int lidx_extract_topk_scores(const float* logits, const int32_t* idx,
  *   [0, min((s+1)/compress_ratio, Skv)).  Only entries in the row's range are
  *   candidates.  Output as lidx_indexer_fwd: indices_out int32 / scores_out
  *   fp32 [rows, topk], sorted by score descending, ties by ascending index,
- *   padded with -1 / -inf.  Limit of this build: visible keys per row <= 4096.
+ *   padded with -1 / -inf.  Limit of this build: Skv <= 65536.
  */
 int lidx_topk_rows(const float* logits, int64_t rows, int64_t S, int64_t Skv,
                    int compress_ratio, const int32_t* ks, const int32_t* ke, int topk,
@@ -167,6 +190,27 @@ int lidx_indexer_scores_v41(const void* q, const void* k, const void* w,
                             const uint8_t* allowed, int64_t B, int64_t S, int64_t Skv,
                             int H, int D, int act, void* scores_out,
                             void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * V4.1 scores and their per-row top-k   [P3 indexer_scores; module docstring:
+ * the top-k / candidate selection runs on these scores].  Scores as
+ * lidx_indexer_scores_v41; then, per row (b,s), the top `topk` of the visible
+ * keys (allowed != 0) by bf16 score, sorted descending, equal scores by
+ * ascending key index; rows with fewer visible keys end with index -1 /
+ * score -inf.
+ *   scores_out      bf16 [B,S,Skv], nullable: NULL keeps the scores in the
+ *                   workspace instead.
+ *   indices_out     int32 [B,S,topk];  topk_scores_out bf16 [B,S,topk].
+ *   workspace       lidx_workspace_bytes(LIDX_OP_TOPK_V41, B,S,Skv,H,D,topk,
+ *                   scores_out != NULL) bytes, 256-byte aligned.
+ *   Visible scores must be finite (they are for finite inputs of this size).
+ *   Limit of this build: Skv <= 65536.
+ */
+int lidx_indexer_topk_v41(const void* q, const void* k, const void* w,
+                          const uint8_t* allowed, int64_t B, int64_t S, int64_t Skv,
+                          int H, int D, int act, int topk, void* scores_out,
+                          int32_t* indices_out, void* topk_scores_out,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * V4 backward through the selected entries   [P1 V4IndexerFunction.backward;
@@ -188,6 +232,19 @@ int lidx_indexer_bwd(const void* q, const void* k, const float* w,
                      void* dq, void* dk, float* dw,
                      void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Backward over explicit per-row ranges (the ranges of lidx_indexer_fwd_ranges):
+ * as lidx_indexer_bwd, with slot t of row (b,s) contributing only when
+ * max(ks[s],0) <= t < min(ke[s],Skv).  A context-parallel rank gets its own
+ * rows' dq and dw and a partial dk; the ranks' partial dk sum to the full dk.
+ */
+int lidx_indexer_bwd_ranges(const void* q, const void* k, const float* w,
+                            const int32_t* idx, const float* grad_scores,
+                            int64_t B, int64_t S, int64_t Skv, int H, int D,
+                            const int32_t* ks, const int32_t* ke, int topk, int act,
+                            int grad_dtype, void* dq, void* dk, float* dw,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
 /* Device scratch the call needs for these sizes, in bytes (0 = none).
  * logits_materialised: 1 if logits_out will be non-NULL (LIDX_OP_INDEXER_FWD). */
 size_t lidx_workspace_bytes(int op, int64_t B, int64_t S, int64_t Skv, int H, int D,
@@ -197,10 +254,26 @@ size_t lidx_workspace_bytes(int op, int64_t B, int64_t S, int64_t Skv, int H, in
  * LIDX_ERR_DEVICE_TIMEOUT) and clears it.  LIDX_ERR_CUDA if the sync fails. */
 int lidx_device_status(void* stream);
 
+/*
+ * Failure-detection controls (no counterpart on the pages).  Every pipeline
+ * wait inside the kernels gives up after a time limit, records
+ * LIDX_ERR_DEVICE_TIMEOUT in the status word and winds its kernel down, so a
+ * stalled pipeline ends the launch instead of hanging the GPU.
+ *   lidx_set_wait_limit_ns  sets that limit for later launches (0 restores the
+ *                           default of 2 s) and returns the previous one.
+ *   lidx_debug_stall_producer  1: later launches of the scoring kernel load
+ *                           nothing, so its waits run out (for tests of the
+ *                           timeout path; outputs are then unspecified); 0:
+ *                           normal operation.  Returns the previous setting.
+ * Both are process-wide and take effect at the next launch.
+ */
+uint64_t lidx_set_wait_limit_ns(uint64_t ns);
+int lidx_debug_stall_producer(int on);
+
 /* Static English description of a status code (never NULL). */
 const char* lidx_status_string(int status);
 
-/* Library version, e.g. 0x000100 for 0.1.0. */
+/* Library version, e.g. 0x000200 for 0.2.0. */
 int lidx_version(void);
 
 #ifdef __cplusplus

@@ -8,12 +8,17 @@ not been built, or no sm_103 device is present, calls raise.
 Functions carry the C names:
 
   lidx_indexer_fwd          V4 forward: causal mask + per-row top-k
+  lidx_indexer_fwd_ranges   V4 forward over explicit per-row [ks, ke) ranges
   lidx_indexer_logits       V4 logits only, causal or explicit [ks, ke) ranges
   lidx_extract_topk_scores  gather of logits at indices
   lidx_topk_rows            per-row top-k of given logits
   lidx_indexer_scores_v41   V4.1 bf16-rounded scores under a visibility mask
+  lidx_indexer_topk_v41     V4.1 scores and their per-row top-k
   lidx_indexer_bwd          backward through the selected entries
-  lidx_workspace_bytes, lidx_device_status, lidx_status_string
+  lidx_indexer_bwd_ranges   the same over explicit per-row ranges
+  lidx_indexer_fwd_noalloc  fused forward with the library's own scratch
+  lidx_workspace_bytes, lidx_device_status, lidx_status_string,
+  lidx_set_wait_limit_ns, lidx_debug_stall_producer
 """
 
 from __future__ import annotations
@@ -31,14 +36,16 @@ LIDX_OK = 0
 STATUS = {0: "LIDX_OK", 1: "LIDX_ERR_NULL", 2: "LIDX_ERR_SHAPE", 3: "LIDX_ERR_ALIGN",
           4: "LIDX_ERR_UNSUPPORTED", 5: "LIDX_ERR_WORKSPACE", 6: "LIDX_ERR_CUDA",
           7: "LIDX_ERR_DEVICE_TIMEOUT", 8: "LIDX_ERR_NO_DEVICE"}
-OP_INDEXER_FWD, OP_INDEXER_BWD, OP_SCORES_V41 = 0, 1, 2
+OP_INDEXER_FWD, OP_INDEXER_BWD, OP_SCORES_V41, OP_TOPK_V41 = 0, 1, 2, 3
 ACT = {"relu": 0, "identity": 1}
 
 # every symbol include/lidx.h declares
-EXPORTS = ("lidx_indexer_fwd", "lidx_indexer_logits", "lidx_extract_topk_scores", "lidx_topk_rows",
-           "lidx_indexer_scores_v41", "lidx_indexer_bwd", "lidx_workspace_bytes",
-           "lidx_device_status", "lidx_status_string", "lidx_version",
-           "lidx_indexer_fwd_noalloc", "lidx_noalloc_scratch_bytes")
+EXPORTS = ("lidx_indexer_fwd", "lidx_indexer_fwd_ranges", "lidx_indexer_logits",
+           "lidx_extract_topk_scores", "lidx_topk_rows", "lidx_indexer_scores_v41",
+           "lidx_indexer_topk_v41", "lidx_indexer_bwd", "lidx_indexer_bwd_ranges",
+           "lidx_workspace_bytes", "lidx_device_status", "lidx_status_string", "lidx_version",
+           "lidx_indexer_fwd_noalloc", "lidx_noalloc_scratch_bytes", "lidx_set_wait_limit_ns",
+           "lidx_debug_stall_producer")
 
 
 class LidxError(RuntimeError):
@@ -65,6 +72,16 @@ def lib() -> C.CDLL:
             P, i64, i32, sz = C.c_void_p, C.c_int64, C.c_int, C.c_size_t
             L.lidx_indexer_fwd.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, i32, i32,
                                            P, P, P, P, P, sz, P]
+            L.lidx_indexer_fwd_ranges.argtypes = [P, P, P, i64, i64, i64, i32, i32, P, P, i32, i32,
+                                                  P, P, P, P, P, sz, P]
+            L.lidx_indexer_topk_v41.argtypes = [P, P, P, P, i64, i64, i64, i32, i32, i32, i32, P, P,
+                                                P, P, sz, P]
+            L.lidx_indexer_bwd_ranges.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, P, P, i32,
+                                                  i32, i32, P, P, P, P, sz, P]
+            L.lidx_set_wait_limit_ns.argtypes = [C.c_uint64]
+            L.lidx_set_wait_limit_ns.restype = C.c_uint64
+            L.lidx_debug_stall_producer.argtypes = [i32]
+            L.lidx_debug_stall_producer.restype = i32
             L.lidx_indexer_logits.argtypes = [P, P, P, i64, i64, i64, i32, i32, i32, P, P, i32,
                                               i32, P, P]
             L.lidx_extract_topk_scores.argtypes = [P, P, i64, i64, i64, i32, P, P]
@@ -83,8 +100,10 @@ def lib() -> C.CDLL:
             L.lidx_status_string.argtypes = [i32]
             L.lidx_status_string.restype = C.c_char_p
             L.lidx_version.restype = i32
-            for name in ("lidx_indexer_fwd", "lidx_indexer_logits", "lidx_extract_topk_scores", "lidx_topk_rows",
-                         "lidx_indexer_scores_v41", "lidx_indexer_bwd", "lidx_device_status"):
+            for name in ("lidx_indexer_fwd", "lidx_indexer_fwd_ranges", "lidx_indexer_logits",
+                         "lidx_extract_topk_scores", "lidx_topk_rows", "lidx_indexer_scores_v41",
+                         "lidx_indexer_topk_v41", "lidx_indexer_bwd", "lidx_indexer_bwd_ranges",
+                         "lidx_device_status"):
                 getattr(L, name).restype = i32
             _lib = L
     return _lib
@@ -129,13 +148,7 @@ def lidx_device_status(stream=None) -> int:
     return int(lib().lidx_device_status(_stream(stream)))
 
 
-def lidx_indexer_fwd(q, k, w, compress_ratio, topk, act="relu", topk_indices=None,
-                     materialise_logits=False, stream=None, out=None, workspace=None):
-    """V4 forward.  q [S,B,H,D] bf16, k [Skv,B,D] bf16, w [S,B,H] fp32.
-
-    Returns (indices [B,S,topk] int32, scores [B,S,topk] fp32, logits or None).
-    ``out`` may hold preallocated (indices, scores, logits) tensors.
-    """
+def _fwd_common(q, k, w, topk, topk_indices, materialise_logits, out, workspace):
     _need(q, "q", torch.bfloat16, 4)
     _need(k, "k", torch.bfloat16, 3)
     _need(w, "w", torch.float32, 3)
@@ -155,11 +168,40 @@ def lidx_indexer_fwd(q, k, w, compress_ratio, topk, act="relu", topk_indices=Non
     ws_bytes = lidx_workspace_bytes(OP_INDEXER_FWD, B, S, Skv, H, D, topk, lg is not None)
     if workspace is None and ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    return (S, B, H, D, Skv), idx, sc, lg, workspace, ws_bytes
+
+
+def lidx_indexer_fwd(q, k, w, compress_ratio, topk, act="relu", topk_indices=None,
+                     materialise_logits=False, stream=None, out=None, workspace=None):
+    """V4 forward.  q [S,B,H,D] bf16, k [Skv,B,D] bf16, w [S,B,H] fp32.
+
+    Returns (indices [B,S,topk] int32, scores [B,S,topk] fp32, logits or None).
+    ``out`` may hold preallocated (indices, scores, logits) tensors.
+    """
+    (S, B, H, D, Skv), idx, sc, lg, workspace, ws_bytes = _fwd_common(
+        q, k, w, topk, topk_indices, materialise_logits, out, workspace)
     rc = lib().lidx_indexer_fwd(_ptr(q), _ptr(k), _ptr(w), B, S, Skv, H, D, compress_ratio, topk,
                                 ACT[act], _ptr(topk_indices), _ptr(lg), _ptr(idx), _ptr(sc),
                                 _ptr(workspace), ws_bytes if workspace is not None else 0,
                                 _stream(stream))
     _check(rc, "lidx_indexer_fwd")
+    return idx, sc, lg
+
+
+def lidx_indexer_fwd_ranges(q, k, w, ks, ke, topk, act="relu", topk_indices=None,
+                            materialise_logits=False, stream=None, out=None, workspace=None):
+    """V4 forward where row (b,s) sees keys [ks[s], ke[s]) (int32 [S] CUDA tensors)."""
+    _need(ks, "ks", torch.int32, 1)
+    _need(ke, "ke", torch.int32, 1)
+    (S, B, H, D, Skv), idx, sc, lg, workspace, ws_bytes = _fwd_common(
+        q, k, w, topk, topk_indices, materialise_logits, out, workspace)
+    if ks.shape[0] != S or ke.shape[0] != S:
+        raise ValueError("ks/ke must have S entries")
+    rc = lib().lidx_indexer_fwd_ranges(_ptr(q), _ptr(k), _ptr(w), B, S, Skv, H, D, _ptr(ks), _ptr(ke),
+                                       topk, ACT[act], _ptr(topk_indices), _ptr(lg), _ptr(idx),
+                                       _ptr(sc), _ptr(workspace),
+                                       ws_bytes if workspace is not None else 0, _stream(stream))
+    _check(rc, "lidx_indexer_fwd_ranges")
     return idx, sc, lg
 
 
@@ -265,9 +307,47 @@ def lidx_indexer_scores_v41(q, k, w, allowed, act="relu", stream=None, out=None,
     return res
 
 
-def lidx_indexer_bwd(q, k, w, idx, grad, compress_ratio, act="relu", stream=None, out=None,
-                     workspace=None):
-    """Gradients (dq [S,B,H,D], dk [Skv,B,D], dw [S,B,H]) fp32."""
+def lidx_indexer_topk_v41(q, k, w, allowed, topk, act="relu", keep_scores=True, stream=None,
+                          out=None, workspace=None):
+    """V4.1 scores and their per-row top-k.  Returns (scores bf16 [B,S,Skv] or
+    None, indices int32 [B,S,topk], top-k scores bf16 [B,S,topk])."""
+    _need(q, "q", torch.bfloat16, 4)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(w, "w", torch.bfloat16, 3)
+    if allowed.dtype not in (torch.bool, torch.uint8):
+        raise TypeError("allowed must be bool or uint8")
+    if not (allowed.is_cuda and allowed.is_contiguous() and allowed.dim() == 3):
+        raise ValueError("allowed must be a contiguous CUDA [B,S,Skv] tensor")
+    B, S, H, D = q.shape
+    Skv = k.shape[1]
+    dev = q.device
+    if out is None:
+        res = torch.empty(B, S, Skv, dtype=torch.bfloat16, device=dev) if keep_scores else None
+        idx = torch.empty(B, S, topk, dtype=torch.int32, device=dev)
+        tsc = torch.empty(B, S, topk, dtype=torch.bfloat16, device=dev)
+    else:
+        res, idx, tsc = out
+    ws_bytes = lidx_workspace_bytes(OP_TOPK_V41, B, S, Skv, H, D, topk, res is not None)
+    if workspace is None and ws_bytes:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    rc = lib().lidx_indexer_topk_v41(_ptr(q), _ptr(k), _ptr(w), _ptr(allowed), B, S, Skv, H, D,
+                                     ACT[act], topk, _ptr(res), _ptr(idx), _ptr(tsc), _ptr(workspace),
+                                     ws_bytes if workspace is not None else 0, _stream(stream))
+    _check(rc, "lidx_indexer_topk_v41")
+    return res, idx, tsc
+
+
+def lidx_set_wait_limit_ns(ns: int) -> int:
+    """Limit of every in-kernel pipeline wait (0: the 2 s default); returns the previous."""
+    return int(lib().lidx_set_wait_limit_ns(int(ns)))
+
+
+def lidx_debug_stall_producer(on: bool) -> int:
+    """Test switch: the scoring kernel's producer loads nothing, so its waits run out."""
+    return int(lib().lidx_debug_stall_producer(int(bool(on))))
+
+
+def _bwd_common(q, k, w, idx, grad, grad_dtype, out, workspace):
     _need(q, "q", torch.bfloat16, 4)
     _need(k, "k", torch.bfloat16, 3)
     _need(w, "w", torch.float32, 3)
@@ -277,17 +357,41 @@ def lidx_indexer_bwd(q, k, w, idx, grad, compress_ratio, act="relu", stream=None
     Skv = k.shape[0]
     topk = idx.shape[2]
     dev = q.device
+    gdt = {torch.float32: 0, torch.bfloat16: 1}[grad_dtype]
     if out is None:
-        dq = torch.empty(S, B, H, D, dtype=torch.float32, device=dev)
-        dk = torch.empty(Skv, B, D, dtype=torch.float32, device=dev)
+        dq = torch.empty(S, B, H, D, dtype=grad_dtype, device=dev)
+        dk = torch.empty(Skv, B, D, dtype=grad_dtype, device=dev)
         dw = torch.empty(S, B, H, dtype=torch.float32, device=dev)
     else:
         dq, dk, dw = out
     ws_bytes = lidx_workspace_bytes(OP_INDEXER_BWD, B, S, Skv, H, D, topk)
     if workspace is None and ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    return (S, B, H, D, Skv, topk, gdt), dq, dk, dw, workspace, ws_bytes
+
+
+def lidx_indexer_bwd_ranges(q, k, w, idx, grad, ks, ke, act="relu", grad_dtype=torch.float32,
+                            stream=None, out=None, workspace=None):
+    """Backward where row (b,s) sees keys [ks[s], ke[s]); dk is this call's partial sum."""
+    _need(ks, "ks", torch.int32, 1)
+    _need(ke, "ke", torch.int32, 1)
+    (S, B, H, D, Skv, topk, gdt), dq, dk, dw, workspace, ws_bytes = _bwd_common(
+        q, k, w, idx, grad, grad_dtype, out, workspace)
+    rc = lib().lidx_indexer_bwd_ranges(_ptr(q), _ptr(k), _ptr(w), _ptr(idx), _ptr(grad), B, S, Skv, H,
+                                       D, _ptr(ks), _ptr(ke), topk, ACT[act], gdt, _ptr(dq), _ptr(dk),
+                                       _ptr(dw), _ptr(workspace),
+                                       ws_bytes if workspace is not None else 0, _stream(stream))
+    _check(rc, "lidx_indexer_bwd_ranges")
+    return dq, dk, dw
+
+
+def lidx_indexer_bwd(q, k, w, idx, grad, compress_ratio, act="relu", grad_dtype=torch.float32,
+                     stream=None, out=None, workspace=None):
+    """Gradients (dq [S,B,H,D], dk [Skv,B,D] in grad_dtype (fp32 or bf16), dw [S,B,H] fp32)."""
+    (S, B, H, D, Skv, topk, gdt), dq, dk, dw, workspace, ws_bytes = _bwd_common(
+        q, k, w, idx, grad, grad_dtype, out, workspace)
     rc = lib().lidx_indexer_bwd(_ptr(q), _ptr(k), _ptr(w), _ptr(idx), _ptr(grad), B, S, Skv, H, D,
-                                compress_ratio, topk, ACT[act], 0, _ptr(dq), _ptr(dk), _ptr(dw),
+                                compress_ratio, topk, ACT[act], gdt, _ptr(dq), _ptr(dk), _ptr(dw),
                                 _ptr(workspace), ws_bytes if workspace is not None else 0,
                                 _stream(stream))
     _check(rc, "lidx_indexer_bwd")

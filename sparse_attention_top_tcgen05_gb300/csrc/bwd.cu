@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     bwd_rows_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                     const float* __restrict__ w, const int32_t* __restrict__ idx,
                     const float* __restrict__ grad, int B, int S, int Skv, int D, int ratio,
+                    const int32_t* __restrict__ ksa, const int32_t* __restrict__ kea,
                     int topk, int act, float* __restrict__ dq, float* __restrict__ dk,
                     float* __restrict__ dw) {
     extern __shared__ __align__(16) float sm[];
@@ -60,8 +61,14 @@ __global__ void __launch_bounds__(kBwdThreads)
 
     for (int r = blockIdx.x; r < B * S; r += gridDim.x) {
         const int b = r / S, s = r % S;
-        const long long ke_ll = (long long)(s + 1) / ratio;
-        const int ke = (int)(ke_ll < Skv ? ke_ll : Skv);
+        int ks = 0, ke;
+        if (ksa) {
+            ks = ksa[s] > 0 ? ksa[s] : 0;
+            ke = kea[s] < Skv ? kea[s] : Skv;
+        } else {
+            const long long ke_ll = (long long)(s + 1) / ratio;
+            ke = (int)(ke_ll < Skv ? ke_ll : Skv);
+        }
         __syncthreads();  // previous row done with shared memory
         for (int e = tid; e < H * D; e += kBwdThreads) {
             const int h = e / D, d = e % D;
@@ -84,7 +91,7 @@ __global__ void __launch_bounds__(kBwdThreads)
             for (int j = tid; j < kBwdJ; j += kBwdThreads) {
                 const int slot = j0 + j;
                 int t = slot < topk ? irow[slot] : -1;
-                if (t < 0 || t >= ke) t = -1;  // padding or outside the causal range
+                if (t < ks || t >= ke) t = -1;  // padding or outside the causal range
                 ts[j] = t;
                 gs[j] = t >= 0 ? grow[slot] : 0.f;
             }
@@ -193,6 +200,7 @@ __global__ void __launch_bounds__(kBwdThreads)
     bwd_rows_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                         const float* __restrict__ w, const int32_t* __restrict__ idx,
                         const float* __restrict__ grad, int B, int S, int Skv, int D, int ratio,
+                        const int32_t* __restrict__ ksa, const int32_t* __restrict__ kea,
                         int topk, int act, float* __restrict__ dq, float* __restrict__ dk,
                         float* __restrict__ dw) {
     static_assert(H % 16 == 0, "H must be a multiple of 16");
@@ -216,8 +224,14 @@ __global__ void __launch_bounds__(kBwdThreads)
 
     for (int r = blockIdx.x; r < B * S; r += gridDim.x) {
         const int b = r / S, s = r % S;
-        const long long ke_ll = (long long)(s + 1) / ratio;
-        const int ke = (int)(ke_ll < Skv ? ke_ll : Skv);
+        int ks = 0, ke;
+        if (ksa) {
+            ks = ksa[s] > 0 ? ksa[s] : 0;
+            ke = kea[s] < Skv ? kea[s] : Skv;
+        } else {
+            const long long ke_ll = (long long)(s + 1) / ratio;
+            ke = (int)(ke_ll < Skv ? ke_ll : Skv);
+        }
         __syncthreads();
         for (int e = tid; e < H * D; e += kBwdThreads) {
             const int h = e / D, d = e % D;
@@ -240,7 +254,7 @@ __global__ void __launch_bounds__(kBwdThreads)
             for (int j = tid; j < kBwdJ; j += kBwdThreads) {
                 const int slot = j0 + j;
                 int t = slot < topk ? irow[slot] : -1;
-                if (t < 0 || t >= ke) t = -1;
+                if (t < ks || t >= ke) t = -1;
                 ts[j] = t;
                 gs[j] = t >= 0 ? grow[slot] : 0.f;
             }
@@ -348,7 +362,7 @@ template <int H>
 static cudaError_t bwd_mma_h(const BwdLaunch& a) {
     const size_t smem = bwd_mma_smem(H, a.D);
     auto kern = bwd_rows_mma_kernel<H>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_smem_attr((const void*)kern, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBwdThreads, smem);
@@ -358,7 +372,7 @@ static cudaError_t bwd_mma_h(const BwdLaunch& a) {
     if (grid > rows) grid = rows;
     kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(
         (const uint16_t*)a.q, (const uint16_t*)a.k, a.w, a.idx, a.grad, a.B, a.S, a.Skv, a.D, a.ratio,
-        a.topk, a.act, a.dq, a.dk, a.dw);
+        a.ks, a.ke, a.topk, a.act, (float*)a.dq, (float*)a.dk, a.dw);
     return cudaGetLastError();
 }
 
@@ -373,7 +387,7 @@ template <int H>
 static cudaError_t bwd_h(const BwdLaunch& a) {
     const size_t smem = bwd_smem(H, a.D);
     auto kern = bwd_rows_kernel<H>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_smem_attr((const void*)kern, (int)smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBwdThreads, smem);
@@ -383,9 +397,13 @@ static cudaError_t bwd_h(const BwdLaunch& a) {
     if (grid > rows) grid = rows;
     kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(
         (const uint16_t*)a.q, (const uint16_t*)a.k, a.w, a.idx, a.grad, a.B, a.S, a.Skv, a.D, a.ratio,
-        a.topk, a.act, a.dq, a.dk, a.dw);
+        a.ks, a.ke, a.topk, a.act, (float*)a.dq, (float*)a.dk, a.dw);
     return cudaGetLastError();
 }
+
+LIDX_STATUS_READER(status_bwd)
+
+size_t bwd_workspace_bytes(int64_t, int64_t, int64_t, int, int, int, int) { return 0; }
 
 cudaError_t bwd_launch(const BwdLaunch& a) {
     // dk is a sum over rows: clear it first (dq and dw are written whole)

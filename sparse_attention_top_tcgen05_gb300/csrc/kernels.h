@@ -27,6 +27,9 @@ struct ScoreParams {
     uint16_t* out16;          // [B,S,Skv] bf16
     const uint8_t* tilemap;   // [B, qtiles, ntk]: 1 where the block has a visible pair
     int ntk;                  // key tiles per row
+    const int32_t* idx_in;    // nullable [B,S,topk]: score these keys instead of selecting
+    uint64_t wait_ns;         // limit of every pipeline wait
+    int debug_stall;          // 1: the TMA producer issues nothing (failure-detection tests)
     // filled by the launcher
     int num_units, qtiles, Skv_pad, swz;
 };
@@ -58,6 +61,9 @@ cudaError_t extract_launch(const float* logits, const int32_t* idx, int64_t rows
 cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, int ratio,
                              const int32_t* ks, const int32_t* ke, int topk, int32_t* out_idx,
                              float* out_sc, cudaStream_t stream);
+// selection over bf16 rows; -inf entries are not candidates (V4.1 scores)
+cudaError_t topk_rows_bf16_launch(const uint16_t* scores, int64_t rows, int Skv, int topk,
+                                  int32_t* out_idx, uint16_t* out_sc, cudaStream_t stream);
 // backward through the selected entries (bwd.cu)
 struct BwdLaunch {
     const void* q;
@@ -65,33 +71,40 @@ struct BwdLaunch {
     const float* w;
     const int32_t* idx;
     const float* grad;
-    int B, S, Skv, H, D, ratio, topk, act;
-    float* dq;
-    float* dk;
+    int B, S, Skv, H, D, ratio, topk, act, grad_dtype;
+    const int32_t* ks;  // nullable with ke: causal ranges from ratio
+    const int32_t* ke;
+    void* dq;           // fp32 or bf16 (grad_dtype)
+    void* dk;
     float* dw;
+    void* workspace;
+    size_t workspace_bytes;
     cudaStream_t stream;
     int num_sms;
 };
 cudaError_t bwd_launch(const BwdLaunch& a);
-
-// forward with given indices (gather.cu)
-struct GatherLaunch {
-    const void* q;
-    const void* k;
-    const float* w;
-    const int32_t* idx;
-    int B, S, Skv, H, D, ratio, topk, act;
-    int32_t* out_idx;
-    float* out_sc;
-    cudaStream_t stream;
-    int num_sms;
-};
-cudaError_t gather_launch(const GatherLaunch& a);
+size_t bwd_workspace_bytes(int64_t B, int64_t S, int64_t Skv, int H, int D, int topk, int num_sms);
 
 cudaError_t pad_launch(int64_t n, int32_t* idx, float* sc, cudaStream_t stream);
+// padding with bf16 scores; and given indices copied with -inf scores
+cudaError_t pad16_launch(int64_t n, int32_t* idx, uint16_t* sc, cudaStream_t stream);
+cudaError_t copy_pad_launch(int64_t n, const int32_t* in, int32_t* idx, float* sc, cudaStream_t stream);
+
+// argument rules of the V4 forward that need no device (api.cu); LIDX_OK or an error
+int check_fwd(const void* q, const void* k, const float* w, int64_t B, int64_t S, int64_t Skv, int H,
+              int D, int compress_ratio, const int32_t* ks, const int32_t* ke, int topk, int act,
+              const int32_t* topk_indices_in, const float* logits_out, const int32_t* indices_out,
+              const float* scores_out);
+
+// host-side state shared by the launchers (api.cu)
+int current_sms();                                   // SM count of the current device
+cudaError_t set_smem_attr(const void* fn, int smem);  // once per (device, kernel, size)
+uint64_t wait_limit_ns();                             // limit of every pipeline wait
+int debug_stall();                                    // failure-detection test switch
 
 // per-TU status readers (see LIDX_STATUS_READER): value, or -1 on a CUDA error
 int status_score_fwd(int clear);
 int status_misc(int clear);
+int status_bwd(int clear);
 
 }  // namespace lidx

@@ -27,9 +27,7 @@ cudaError_t extract_launch(const float* logits, const int32_t* idx, int64_t rows
                            int topk, float* out, cudaStream_t stream) {
     const int64_t n = rows * (int64_t)topk;
     if (n == 0) return cudaSuccess;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = current_sms();
     int64_t blocks = (n + 255) / 256;
     const int64_t cap = (int64_t)sms * 8;
     if (blocks > cap) blocks = cap;
@@ -55,6 +53,42 @@ cudaError_t pad_launch(int64_t n, int32_t* idx, float* sc, cudaStream_t stream) 
     return cudaGetLastError();
 }
 
+// The same with bf16 scores (-inf = 0xFF80).
+__global__ void pad16_kernel(int64_t n, int32_t* __restrict__ idx, uint16_t* __restrict__ sc) {
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        idx[e] = -1;
+        sc[e] = 0xFF80u;
+    }
+}
+
+cudaError_t pad16_launch(int64_t n, int32_t* idx, uint16_t* sc, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    pad16_kernel<<<(unsigned)blocks, 256, 0, stream>>>(n, idx, sc);
+    return cudaGetLastError();
+}
+
+// Given indices with no keys to score: indices copied through, scores -inf.
+__global__ void copy_pad_kernel(int64_t n, const int32_t* __restrict__ in, int32_t* __restrict__ idx,
+                                float* __restrict__ sc) {
+    const float ninf = __int_as_float(0xff800000);
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        idx[e] = in[e];
+        sc[e] = ninf;
+    }
+}
+
+cudaError_t copy_pad_launch(int64_t n, const int32_t* in, int32_t* idx, float* sc, cudaStream_t stream) {
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    copy_pad_kernel<<<(unsigned)blocks, 256, 0, stream>>>(n, in, idx, sc);
+    return cudaGetLastError();
+}
+
 // Standalone selection: each CTA (kTopkRowThreads threads) takes rows in turn.
 constexpr int kTopkRowThreads = 256;
 
@@ -76,28 +110,61 @@ __global__ void __launch_bounds__(kTopkRowThreads)
             hi = ke[s] < Skv ? ke[s] : Skv;
             if (hi < lo) hi = lo;
         }
-        row_topk<kTopkRowThreads>(logits + r * (int64_t)Skv, lo, hi, topk, out_idx + r * topk,
-                                  out_sc + r * topk, sm, threadIdx.x, 1);
+        row_topk<kTopkRowThreads, false, float>(logits + r * (int64_t)Skv, lo, hi, topk,
+                                                out_idx + r * topk, out_sc + r * topk, sm,
+                                                threadIdx.x, 1);
     }
+}
+
+// Selection over bf16 score rows in which -inf marks a key that is not
+// visible (the V4.1 scorer's output): candidates are the finite entries.
+__global__ void __launch_bounds__(kTopkRowThreads)
+    topk_rows_bf16_kernel(const uint16_t* __restrict__ scores, int64_t rows, int Skv, int topk,
+                          int32_t* __restrict__ out_idx, uint16_t* __restrict__ out_sc) {
+    extern __shared__ uint8_t smem_raw[];
+    TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x)
+        row_topk<kTopkRowThreads, true, uint16_t>(scores + r * (int64_t)Skv, 0, Skv, topk,
+                                                  out_idx + r * topk, out_sc + r * topk, sm,
+                                                  threadIdx.x, 1);
+}
+
+template <class K>
+static cudaError_t topk_grid(K kern, int64_t rows, int* grid_out, int* smem_out) {
+    const int sms = current_sms();
+    const int smem = (int)sizeof(TopkSmem);
+    cudaError_t e = set_smem_attr((const void*)kern, smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTopkRowThreads, smem);
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (int64_t)sms * per_sm;
+    if (grid > rows) grid = rows;
+    *grid_out = (int)grid;
+    *smem_out = smem;
+    return cudaSuccess;
 }
 
 cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, int ratio,
                              const int32_t* ks, const int32_t* ke, int topk, int32_t* out_idx,
                              float* out_sc, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int smem = (int)sizeof(TopkSmem);
-    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    int grid = 0, smem = 0;
+    cudaError_t e = topk_grid(topk_rows_kernel, rows, &grid, &smem);
     if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_rows_kernel, kTopkRowThreads, smem);
-    if (per_sm < 1) per_sm = 1;
-    int64_t grid = (int64_t)sms * per_sm;
-    if (grid > rows) grid = rows;
     topk_rows_kernel<<<(unsigned)grid, kTopkRowThreads, smem, stream>>>(logits, rows, S, Skv, ratio, ks,
                                                                         ke, topk, out_idx, out_sc);
+    return cudaGetLastError();
+}
+
+cudaError_t topk_rows_bf16_launch(const uint16_t* scores, int64_t rows, int Skv, int topk,
+                                  int32_t* out_idx, uint16_t* out_sc, cudaStream_t stream) {
+    if (rows == 0) return cudaSuccess;
+    int grid = 0, smem = 0;
+    cudaError_t e = topk_grid(topk_rows_bf16_kernel, rows, &grid, &smem);
+    if (e != cudaSuccess) return e;
+    topk_rows_bf16_kernel<<<(unsigned)grid, kTopkRowThreads, smem, stream>>>(scores, rows, Skv, topk,
+                                                                             out_idx, out_sc);
     return cudaGetLastError();
 }
 

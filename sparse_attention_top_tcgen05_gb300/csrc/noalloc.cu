@@ -18,7 +18,9 @@
 // call before any stream capture.  All calls share the one array: calls that
 // overlap on the GPU (different streams, or different host threads) race on it
 // and must be serialised by the caller.  The kernel writes every scratch entry
-// it later reads, so nothing has to be cleared between calls.
+// it later reads, so nothing has to be cleared between calls.  The looked-up
+// address is kept for the life of the process: a caller that resets a device
+// (cudaDeviceReset) must not call this entry point on that device again.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -59,7 +61,10 @@ extern "C" int lidx_indexer_fwd_noalloc(const void* q, const void* k, const floa
                                         int64_t S, int64_t Skv, int H, int D, int compress_ratio,
                                         int topk, int act, int32_t* indices_out, float* scores_out,
                                         void* stream) {
-    // the same rules as lidx_indexer_fwd apply; only the scratch source differs
+    // the same rules as lidx_indexer_fwd apply, checked first; only the scratch source differs
+    const int rc0 = lidx::check_fwd(q, k, w, B, S, Skv, H, D, compress_ratio, nullptr, nullptr, topk,
+                                    act, nullptr, nullptr, indices_out, scores_out);
+    if (rc0 != LIDX_OK) return rc0;
     const size_t need = lidx_workspace_bytes(LIDX_OP_INDEXER_FWD, B, S, Skv, H, D, topk, 0);
     if (need > lidx::kNoAllocScratchBytes) return LIDX_ERR_WORKSPACE;  // beyond the static array
     void* scratch = nullptr;

@@ -257,6 +257,23 @@ __device__ __forceinline__ float head_sum_v41(const uint32_t (&r)[NR], int c0, c
     }
 }
 
+// Given-index mode ("tilelang_indexer" page, forward with topk_indices): the
+// scores of the row's given keys are read back from its swept row buffer;
+// a key outside the row's visible range [lo, hi) scores -inf.  Indices are
+// copied through.  Ends with a group barrier like row_topk.
+template <int NT>
+__device__ __forceinline__ void row_gather(const float* row, int lo, int hi, const int32_t* idx,
+                                           int topk, int32_t* out_idx, float* out_sc, int tid,
+                                           int bar_id) {
+    const float ninf = __int_as_float(0xff800000);
+    for (int j = tid; j < topk; j += NT) {
+        const int t = idx[j];
+        out_idx[j] = t;
+        out_sc[j] = (t >= lo && t < hi) ? row[t] : ninf;
+    }
+    named_bar_sync(bar_id, NT);
+}
+
 template <int H, bool V41>
 __global__ void __launch_bounds__(kThreads, 1)
     score_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -316,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (lane == 0 && !p.debug_stall) {
             int kcount = 0, qcount = 0;
             bool ok = true;
             for (int i = 0; ok; ++i) {
@@ -325,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u < 0) continue;
                 const Unit un = make_unit<QT, V41>(p, u);
                 if (un.hi_t <= un.lo_t) continue;
-                if (!(ok = mbar_wait(q_empty, (qcount & 1) ^ 1))) break;
+                if (!(ok = mbar_wait(q_empty, (qcount & 1) ^ 1, p.wait_ns))) break;
                 ++qcount;
                 mbar_arrive_expect_tx(q_full, kN * p.D * 2);
                 for (int kb = 0; kb < nkb; ++kb)
@@ -350,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kt = un.lo_t; kt < un.hi_t; ++kt) {
                     if (!tile_active<V41>(p, un, kt)) continue;
                     const int st = kcount % kStages;
-                    if (!(ok = mbar_wait(k_empty + st, ((kcount / kStages) & 1) ^ 1))) break;
+                    if (!(ok = mbar_wait(k_empty + st, ((kcount / kStages) & 1) ^ 1, p.wait_ns))) break;
                     ++kcount;
                     uint8_t* dst = sK + st * kM * p.D * 2;
                     mbar_arrive_expect_tx(k_full + st, kM * p.D * 2);
@@ -390,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (u < 0) continue;
                 const Unit un = make_unit<QT, V41>(p, u);
                 if (un.hi_t <= un.lo_t) continue;
-                if (!(ok = mbar_wait(q_full, qcount & 1))) break;
+                if (!(ok = mbar_wait(q_full, qcount & 1, p.wait_ns))) break;
                 ++qcount;
                 tc_fence_after();
                 for (int kt = un.lo_t; kt < un.hi_t; ++kt) {
@@ -399,9 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t kph = (kcount / kStages) & 1, aph = ((tcount >> 1) & 1) ^ 1;
                     ++kcount;
                     ++tcount;
-                    if (!(ok = mbar_wait(acc_empty + acc, aph))) break;
+                    if (!(ok = mbar_wait(acc_empty + acc, aph, p.wait_ns))) break;
                     tc_fence_after();
-                    if (!(ok = mbar_wait(k_full + st, kph))) break;
+                    if (!(ok = mbar_wait(k_full + st, kph, p.wait_ns))) break;
                     tc_fence_after();
                     const uint32_t d = tmem_base + acc * kN;
 #pragma unroll
@@ -453,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!tile_active<V41>(p, un, kt)) continue;  // written as -inf by the mask pass
                     const int t = kt * kM + row_t;
                     const int acc = tcount & 1;
-                    if (!(ok = mbar_wait(acc_full + acc, (tcount >> 1) & 1))) break;
+                    if (!(ok = mbar_wait(acc_full + acc, (tcount >> 1) & 1, p.wait_ns))) break;
                     ++tcount;
                     tc_fence_after();
                     auto store16 = [&](int ql, float v) {
@@ -497,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (select) {
                 // the top-k group must have finished the tile that last used slot rb
                 // (this also keeps the row barriers at most one phase apart)
-                if (!(ok = mbar_wait(rows_empty + rb, ((ucount >> 1) & 1) ^ 1))) break;
+                if (!(ok = mbar_wait(rows_empty + rb, ((ucount >> 1) & 1) ^ 1, p.wait_ns))) break;
                 if (!materialise)
                     rows = p.scratch + ((size_t)blockIdx.x * 2 + rb) * p.scratch_stride_cta;
             }
@@ -530,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
                 const int acc = tcount & 1;
-                if (!(ok = mbar_wait(acc_full + acc, (tcount >> 1) & 1))) break;
+                if (!(ok = mbar_wait(acc_full + acc, (tcount >> 1) & 1, p.wait_ns))) break;
                 ++tcount;
                 tc_fence_after();
                 auto store = [&](int ql, float v) {
@@ -604,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 un = make_unit<QT, V41>(p, u);
                 ++ucount;
-                ok = mbar_wait(rows_full + (ucount & 1), (ucount >> 1) & 1);
+                ok = mbar_wait(rows_full + (ucount & 1), (ucount >> 1) & 1, p.wait_ns);
             }
             if (!more || !ok) break;
             const int rb = uc & 1;
@@ -617,8 +634,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        ? p.logits + ((size_t)un.b * p.S + s) * p.Skv
                                        : p.scratch + ((size_t)blockIdx.x * 2 + rb) * p.scratch_stride_cta +
                                              (size_t)ql * p.Skv_pad;
-                row_topk<kTopkGroupThreads>(row, lo, hi, p.topk, p.out_idx + orow, p.out_sc + orow, sTg,
-                                            gtid, kTopkBar + grp);  // ends with a group barrier
+                if (p.idx_in)
+                    row_gather<kTopkGroupThreads>(row, lo, hi, p.idx_in + orow, p.topk, p.out_idx + orow,
+                                                  p.out_sc + orow, gtid, kTopkBar + grp);
+                else
+                    row_topk<kTopkGroupThreads, false, float>(row, lo, hi, p.topk, p.out_idx + orow,
+                                                              p.out_sc + orow, sTg, gtid,
+                                                              kTopkBar + grp);  // ends with a group barrier
             }
             if (gtid == 0) mbar_arrive(rows_empty + rb);  // this row's slot entry is free
         }
@@ -663,7 +685,7 @@ template <int H, bool V41>
 static cudaError_t launch_h(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                             int smem, int grid) {
     auto kern = score_fwd_kernel<H, V41>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = set_smem_attr((const void*)kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, a.p);
     return cudaGetLastError();
@@ -696,6 +718,8 @@ size_t score_scratch_bytes(int64_t S, int64_t Skv, int H, int num_sms) {
 
 int score_fwd_launch(ScoreLaunch& a) {
     ScoreParams& p = a.p;
+    p.wait_ns = wait_limit_ns();
+    p.debug_stall = debug_stall();
     const int QT = kN / p.H;
     p.swz = (p.D % 64 == 0) ? 128 : (p.D % 32 == 0 ? 64 : 32);
     p.qtiles = (p.S + QT - 1) / QT;
@@ -719,6 +743,8 @@ int score_fwd_launch(ScoreLaunch& a) {
 // mask pass, which also wrote -inf for every block it marked empty.
 int score_v41_launch(ScoreLaunch& a) {
     ScoreParams& p = a.p;
+    p.wait_ns = wait_limit_ns();
+    p.debug_stall = debug_stall();
     if (p.H < 1 || p.H > 128 || (p.H & (p.H - 1))) return -2;
     const int QT = kN / p.H;
     p.swz = (p.D % 64 == 0) ? 128 : (p.D % 32 == 0 ? 64 : 32);

@@ -118,9 +118,7 @@ cudaError_t v41_mask_launch(const uint8_t* allowed, uint16_t* out, uint8_t* tile
     const int qtiles = (S + QT - 1) / QT, ntk = (Skv + 127) / 128;
     const int64_t units = (int64_t)B * qtiles;
     if (units == 0 || ntk == 0) return cudaSuccess;
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const int sms = current_sms();
     int64_t grid = (int64_t)sms * 8;
     if (grid > units) grid = units;
     if ((Skv & 15) == 0 && ((((uintptr_t)allowed) | ((uintptr_t)out)) & 15) == 0)

@@ -35,7 +35,7 @@ def test_library_exports_every_header_symbol(L):
 
 
 def test_version_and_status_strings(L):
-    assert L.lidx_version() == 0x000100
+    assert L.lidx_version() == 0x000200
     for code in range(0, 9):
         s = lidx.lidx_status_string(code)
         assert s and s != "unknown status"
@@ -64,7 +64,38 @@ def test_argument_validation_without_gpu(L):
     assert _fwd(L, B=0) == 2
     assert _fwd(L, act=5) == 2
     assert _fwd(L, q=18) == 3                         # misaligned
-    assert _fwd(L, Skv=5000) == 4                     # beyond this build's selection limit
+    assert _fwd(L, Skv=70000) == 4                    # beyond this build's selection span
+    assert _fwd(L, Skv=70000, tin=16) != 4            # no selection with given indices
+    assert _fwd(L, B=1 << 16, S=1 << 16) == 2         # rows (b, s) must fit an int
+
+
+def test_new_entry_points_validate_without_gpu(L):
+    P = C.c_void_p
+    # explicit ranges need both arrays
+    rc = L.lidx_indexer_fwd_ranges(P(16), P(16), P(16), 1, 8, 4, 8, 32, None, P(16), 2, 0, None, None,
+                                   P(16), P(16), None, 0, None)
+    assert rc == 1
+    # V4.1 top-k: topk 0 and a misaligned query pointer are rejected before any launch
+    args = [P(16), P(16), P(16), P(16), 1, 8, 64, 8, 32, 0]
+    assert L.lidx_indexer_topk_v41(*args, 0, None, P(16), P(16), None, 0, None) == 2
+    args[0] = P(18)
+    assert L.lidx_indexer_topk_v41(*args, 4, None, P(16), P(16), None, 0, None) == 3
+    # backward ranges need both arrays; grad_dtype outside {0, 1} is a shape error
+    rc = L.lidx_indexer_bwd_ranges(P(16), P(16), P(16), P(16), P(16), 1, 8, 4, 8, 32, P(16), None, 2,
+                                   0, 0, P(16), P(16), P(16), None, 0, None)
+    assert rc == 1
+    rc = L.lidx_indexer_bwd(P(16), P(16), P(16), P(16), P(16), 1, 8, 4, 8, 32, 4, 2, 0, 7, P(16),
+                            P(16), P(16), None, 0, None)
+    assert rc == 2
+
+
+def test_wait_limit_and_stall_switch_round_trip(L):
+    old = lidx.lidx_set_wait_limit_ns(1000)
+    assert old == 2_000_000_000
+    assert lidx.lidx_set_wait_limit_ns(0) == 1000          # 0 restores the default
+    assert lidx.lidx_set_wait_limit_ns(0) == 2_000_000_000
+    assert lidx.lidx_debug_stall_producer(True) == 0
+    assert lidx.lidx_debug_stall_producer(False) == 1
 
 
 def test_workspace_sizes(L):

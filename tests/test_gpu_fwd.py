@@ -217,3 +217,66 @@ def test_given_indices_score_only_those_pairs(H, D, B, S, Skv, ratio, topk):
         assert lidx.lidx_device_status() == 0
         assert np.array_equal(oi.cpu().numpy(), idx)
         assert_scores_close(osc.cpu().numpy().reshape(B * S, topk), ref, "given-index scores")
+
+
+def test_fused_forward_beyond_one_selection_window():
+    """Rows with more visible keys than one shared-memory window of candidates
+    (Skv 9000, ratio 1): the fused and materialised paths agree, the selection
+    equals the exact top-k of the kernel's own logits, and sampled rows agree
+    with the oracle."""
+    g = np.random.default_rng(21)
+    S, B, H, D, Skv, topk = 9100, 1, 8, 32, 9000, 4500
+    q = workloads.to_bf16(g.standard_normal((S, B, H, D)).astype(np.float32) / np.sqrt(D))
+    k = workloads.to_bf16(g.standard_normal((Skv, B, D)).astype(np.float32) / np.sqrt(D))
+    w = torch.from_numpy((g.standard_normal((S, B, H)) / np.sqrt(H)).astype(np.float32))
+    rows = np.concatenate([np.arange(0, S, 397), [4499, 4500, 8999, S - 1]])
+    i1, s1, _ = full_check(q, k, w, 1, topk, materialise=True, rows=rows)
+    i2, s2, _ = run_fwd(q, k, w, 1, topk, False)
+    assert np.array_equal(i1, i2) and np.array_equal(s1, s2)
+
+
+def test_given_indices_without_keys_are_copied():
+    g = np.random.default_rng(6)
+    S, B, H, D, topk = 20, 2, 8, 32, 5
+    q = workloads.to_bf16(g.standard_normal((S, B, H, D)).astype(np.float32))
+    k = workloads.to_bf16(np.zeros((0, B, D), np.float32))
+    w = torch.ones(S, B, H)
+    idx = torch.from_numpy(g.integers(-2, 9, (B, S, topk)).astype(np.int32))
+    qd, kd, wd = cuda(q, k, w)
+    oi, osc, _ = lidx.lidx_indexer_fwd(qd, kd, wd, 4, topk, topk_indices=idx.to(DEV))
+    torch.cuda.synchronize()
+    assert np.array_equal(oi.cpu().numpy(), idx.numpy()) and np.isneginf(osc.cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("ranks", [2, 3])
+def test_context_parallel_shards_on_the_cuda_path(ranks):
+    """Host-simulated context-parallel ranks: each holds a contiguous shard of
+    query rows (global positions p0..p0+S_r) and every compressed key, and calls
+    the library with its own causal ranges.  The shards' forward outputs
+    concatenate to the unsharded call bit for bit; their dq and dw equal the
+    unsharded ones, and their partial dk sum to the full dk."""
+    wl = workloads.WORKLOADS["c4_fwd"].with_(S=2048, Skv=512, topk=256)
+    q, k, w = workloads.v4_inputs(wl, 4)
+    qd, kd, wd = cuda(q, k, w)
+    S, ratio, topk = wl.S, wl.ratio, wl.topk
+    full_i, full_s, _ = lidx.lidx_indexer_fwd(qd, kd, wd, ratio, topk)
+    grad = workloads.grad_scores(1, S, topk, 4).to(DEV)
+    fdq, fdk, fdw = lidx.lidx_indexer_bwd(qd, kd, wd, full_i, grad, ratio)
+    cuts = np.linspace(0, S, ranks + 1).astype(int)
+    dk_sum = torch.zeros_like(fdk)
+    for r in range(ranks):
+        p0, p1 = int(cuts[r]), int(cuts[r + 1])
+        pos = np.arange(p0, p1)
+        ks = torch.zeros(p1 - p0, dtype=torch.int32, device=DEV)
+        ke = torch.from_numpy(np.minimum((pos + 1) // ratio, wl.Skv).astype(np.int32)).to(DEV)
+        qs, ws_ = qd[p0:p1].contiguous(), wd[p0:p1].contiguous()
+        i_r, s_r, _ = lidx.lidx_indexer_fwd_ranges(qs, kd, ws_, ks, ke, topk)
+        assert torch.equal(i_r, full_i[:, p0:p1]) and torch.equal(s_r, full_s[:, p0:p1])
+        dq_r, dk_r, dw_r = lidx.lidx_indexer_bwd_ranges(qs, kd, ws_, i_r, grad[:, p0:p1].contiguous(),
+                                                        ks, ke)
+        assert torch.equal(dq_r, fdq[p0:p1]) and torch.equal(dw_r, fdw[p0:p1])
+        dk_sum += dk_r
+    torch.cuda.synchronize()
+    assert lidx.lidx_device_status() == 0
+    err = (dk_sum - fdk).abs().max().item()
+    assert err <= 1e-5 * fdk.abs().max().item(), err

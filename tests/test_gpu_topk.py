@@ -38,6 +38,14 @@ def rows_case(kind, S, Skv, seed):
         x = (g.standard_cauchy((S, Skv)) * 10).astype(np.float32)
     elif kind == "tiny_range":  # values differing in the last bits only
         x = (1.0 + g.integers(0, 64, (S, Skv)) * 2.0 ** -23).astype(np.float32)
+    elif kind == "zero_pad":  # keys past a short prefix are zero: most scores exactly 0
+        x = g.standard_normal((S, Skv)).astype(np.float32)
+        x[:, Skv // 8:] = 0.0
+    elif kind == "two_values":  # two values only: buckets larger than a shared-memory window
+        x = np.where(g.random((S, Skv)) < 0.5, 1.0, -2.0).astype(np.float32)
+    elif kind == "band":  # one outlier; the rest distinct values in a narrow band
+        x = (1.0 + g.random((S, Skv)) * 1e-4).astype(np.float32)
+        x[:, 3 % Skv] = -1e30
     else:
         raise ValueError(kind)
     return x
@@ -51,6 +59,28 @@ def test_topk_rows_bit_exact(kind, S, Skv, ratio, topk):
     idx, sc = lidx.lidx_topk_rows(lg.reshape(1, S, Skv), topk, compress_ratio=ratio)
     torch.cuda.synchronize()
     ks, ke = oracle.causal_ranges(S, Skv, ratio)
+    oidx, osc = oracle.topk_rows(x.astype(np.float64), S, ks, ke, topk, np.arange(S))
+    assert np.array_equal(idx.cpu().numpy().reshape(S, topk), oidx)
+    assert np.array_equal(sc.cpu().numpy().reshape(S, topk).astype(np.float64), osc)
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties", "const", "outlier", "heavy", "tiny_range",
+                                  "zero_pad", "two_values", "band"])
+@pytest.mark.parametrize("S,Skv,topk", [(40, 8192, 2048), (24, 16384, 6000), (9, 20000, 19000)])
+def test_topk_rows_long_rows_bit_exact(kind, S, Skv, topk):
+    """Rows longer than one shared-memory window of candidates (several
+    windows, refined buckets, all-equal items) select exactly what the oracle
+    selects.  Explicit ranges: the first half of the rows grow from 1 key to
+    the full width, the rest see the full width."""
+    x = rows_case(kind, S, Skv, S * 7 + Skv)
+    lg = torch.from_numpy(x).to(DEV)
+    ks = np.zeros(S, np.int32)
+    ke = np.full(S, Skv, np.int32)
+    ke[: S // 2] = np.linspace(1, Skv, S // 2).astype(np.int32)
+    idx, sc = lidx.lidx_topk_rows(lg.reshape(1, S, Skv), topk, ks=torch.from_numpy(ks).to(DEV),
+                                  ke=torch.from_numpy(ke).to(DEV))
+    torch.cuda.synchronize()
+    assert lidx.lidx_device_status() == 0
     oidx, osc = oracle.topk_rows(x.astype(np.float64), S, ks, ke, topk, np.arange(S))
     assert np.array_equal(idx.cpu().numpy().reshape(S, topk), oidx)
     assert np.array_equal(sc.cpu().numpy().reshape(S, topk).astype(np.float64), osc)

@@ -132,3 +132,71 @@ def test_all_false_and_all_true():
     full = torch.ones(B, S, Skv, dtype=torch.bool)
     check(run(q, k, w, full).reshape(B * S, Skv), oracle.scores_v41_rows(q, k, w, full), full,
           bound=flip_bound(q, k, w))
+
+
+# ------------------------------------------------------------------ V4.1 top-k
+def run_topk(q, k, w, allowed, topk, act="relu"):
+    sc, idx, tsc = lidx.lidx_indexer_topk_v41(q.to(DEV), k.to(DEV), w.to(DEV), allowed.to(DEV), topk,
+                                              act=act)
+    torch.cuda.synchronize()
+    assert lidx.lidx_device_status() == 0
+    return sc.float().cpu().numpy(), idx.cpu().numpy(), tsc.float().cpu().numpy()
+
+
+def check_topk_on_own_scores(sc, idx, tsc, allowed, topk):
+    """The selection equals the oracle's top-k of the kernel's own bf16 scores
+    over the visible keys, bit for bit (scores are exact bf16 values)."""
+    B, S, Skv = sc.shape
+    al = allowed.numpy().reshape(B * S, Skv)
+    oidx, osc = oracle.topk_masked_rows(sc.reshape(B * S, Skv).astype(np.float64), al, topk)
+    assert np.array_equal(idx.reshape(B * S, topk), oidx)
+    assert np.array_equal(tsc.reshape(B * S, topk).astype(np.float64), osc)
+
+
+def test_topk_v41_packed_documents_full_size():
+    """The V4.1 workload's shape (Skv 8192): bf16 scores as lidx_indexer_scores_v41,
+    then the per-row top-512 over the visible keys."""
+    wl = workloads.WORKLOADS["v41_packed"]
+    q, k, w, allowed = workloads.v41_inputs(wl, 0)
+    topk = wl.topk
+    sc, idx, tsc = run_topk(q, k, w, allowed, topk)
+    ref = run(q, k, w, allowed)
+    assert np.array_equal(sc.reshape(ref.shape), ref)  # same scores as the scorer alone
+    check_topk_on_own_scores(sc, idx, tsc, allowed, topk)
+    n = allowed.numpy().reshape(wl.B * wl.S, wl.Skv).sum(1)
+    assert (n > topk).any() and (n < topk).any()  # both selected and padded rows occur
+
+
+@pytest.mark.parametrize("B,S,Skv,H,D,density,topk", [
+    (1, 300, 257, 64, 128, 0.5, 100),   # rows not 16-byte aligned (bf16, Skv odd)
+    (2, 77, 1000, 16, 64, 0.05, 64),
+    (1, 64, 130, 1, 16, 0.9, 200),      # topk above every row's visible count
+    (1, 33, 272, 4, 16, 0.0, 8),        # nothing visible
+    (1, 40, 9000, 8, 32, 0.7, 4000),    # several candidate windows per row
+])
+def test_topk_v41_shapes(B, S, Skv, H, D, density, topk):
+    g = np.random.default_rng(S + Skv + topk)
+    q = workloads.to_bf16(g.standard_normal((B, S, H, D)).astype(np.float32) / np.sqrt(D))
+    k = workloads.to_bf16(g.standard_normal((B, Skv, D)).astype(np.float32) / np.sqrt(D))
+    w = workloads.to_bf16(g.standard_normal((B, S, H)).astype(np.float32) / np.sqrt(H))
+    allowed = torch.from_numpy(g.random((B, S, Skv)) < density)
+    sc, idx, tsc = run_topk(q, k, w, allowed, topk)
+    check_topk_on_own_scores(sc, idx, tsc, allowed, topk)
+    # and the scores themselves are the oracle's within the scorer's tolerance
+    check(sc.reshape(B * S, Skv), oracle.scores_v41_rows(q, k, w, allowed), allowed,
+          bound=flip_bound(q, k, w))
+
+
+def test_topk_v41_without_kept_scores_matches():
+    g = np.random.default_rng(3)
+    B, S, Skv, H, D, topk = 1, 128, 640, 32, 64, 50
+    q = workloads.to_bf16(g.standard_normal((B, S, H, D)).astype(np.float32) / 8)
+    k = workloads.to_bf16(g.standard_normal((B, Skv, D)).astype(np.float32) / 8)
+    w = workloads.to_bf16(g.standard_normal((B, S, H)).astype(np.float32) / 4)
+    allowed = torch.from_numpy(g.random((B, S, Skv)) < 0.4)
+    sc, idx, tsc = run_topk(q, k, w, allowed, topk)
+    none, idx2, tsc2 = lidx.lidx_indexer_topk_v41(q.to(DEV), k.to(DEV), w.to(DEV), allowed.to(DEV),
+                                                  topk, keep_scores=False)
+    assert none is None
+    assert np.array_equal(idx2.cpu().numpy(), idx)
+    assert np.array_equal(tsc2.float().cpu().numpy(), tsc)

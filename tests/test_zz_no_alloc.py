@@ -78,3 +78,44 @@ def test_noalloc_rejects_sizes_beyond_its_array(L):
     assert rc == 5  # LIDX_ERR_WORKSPACE, nothing launched
     torch.cuda.synchronize()
     assert (idx == 7).all()
+
+
+def test_noalloc_checks_arguments_before_its_size_limit(L):
+    """A bad shape is reported as a shape error even when the call would also
+    be too large for the array."""
+    q = torch.zeros(64, 1, 8, 32, dtype=torch.bfloat16, device=DEV)
+    k = torch.zeros(4096, 1, 32, dtype=torch.bfloat16, device=DEV)
+    w = torch.zeros(64, 1, 8, device=DEV)
+    idx = torch.empty(1, 64, 16, dtype=torch.int32, device=DEV)
+    sc = torch.empty(1, 64, 16, device=DEV)
+    P = lambda t: C.c_void_p(t.data_ptr())
+    stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # D = 24 is not a multiple of 16
+    rc = L.lidx_indexer_fwd_noalloc(P(q), P(k), P(w), 1, 64, 4096, 8, 24, 4, 16, 0, P(idx), P(sc), stream)
+    assert rc == 2  # LIDX_ERR_SHAPE
+    rc = L.lidx_indexer_fwd_noalloc(P(q), P(k), P(w), 1, 64, 4096, 8, 32, 0, 16, 0, P(idx), P(sc), stream)
+    assert rc == 2  # compress_ratio 0
+
+
+def test_noalloc_at_the_edge_of_its_array(L):
+    """The largest key count whose scratch fits the array on this device runs
+    and matches the workspace entry point; one key more is rejected."""
+    limit = L.lidx_noalloc_scratch_bytes()
+    H, D = 8, 32
+    fits = [s for s in range(128, 4097, 128)
+            if lidx.lidx_workspace_bytes(lidx.OP_INDEXER_FWD, 1, 1, s, H, D, 16) <= limit]
+    Skv = max(fits)
+    assert lidx.lidx_workspace_bytes(lidx.OP_INDEXER_FWD, 1, 1, Skv + 1, H, D, 16) > limit
+    wl = workloads.WORKLOADS["tiny"].with_(S=Skv + 60, Skv=Skv, H=H, D=D, ratio=1, topk=40)
+    q, k, w = _inputs(5, wl)
+    rc, idx, sc = _noalloc(L, q, k, w, 1, wl.topk)
+    assert rc == 0, lidx.lidx_status_string(rc)
+    ridx, rsc, _ = lidx.lidx_indexer_fwd(q, k, w, 1, wl.topk)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, ridx) and torch.equal(sc, rsc)
+    wl2 = wl.with_(Skv=Skv + 1)
+    q2, k2, w2 = _inputs(6, wl2)
+    rc, idx2, _ = _noalloc(L, q2, k2, w2, 1, wl2.topk)
+    assert rc == 5  # LIDX_ERR_WORKSPACE, nothing launched
+    torch.cuda.synchronize()
+    assert (idx2 == 7).all()

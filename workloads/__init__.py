@@ -11,7 +11,8 @@ Distributions follow the five workloads the indexer is measured on:
 * ``tiny``       B=1 S=256  H=8  D=32  ratio 4, Skv=64,   topk=16,  q,k ~ N(0,1)
 * ``c4_fwd``     B=1 S=4096 H=64 D=128 ratio 4, Skv=1024, topk=512, q,k ~ N(0,1/D)
 * ``long_fused`` B=2 S=16384 H=64 D=128 ratio 4, Skv=4096, topk=2048
-* ``v41_packed`` B=1 S=8192 Skv=8192 H=64 D=128, packed documents, query offset 24576
+* ``v41_packed`` B=1 S=8192 Skv=8192 H=64 D=128, packed documents, query offset 24576;
+  the selection on its scores keeps topk=512 per row
 * ``bwd``        B=1 S=8192 H=64 D=128 ratio 4, Skv=2048, topk=1024
 
 Weights are N(0,1)/sqrt(H).  Values are drawn in float32 and rounded to bf16
@@ -65,7 +66,7 @@ WORKLOADS = {
                  qk_std=1.0 / math.sqrt(128), w_std=1.0 / 8, materialise_logits=True),
     "long_fused": _w("long_fused", B=2, S=16384, H=64, D=128, Skv=4096, ratio=4, topk=2048,
                      qk_std=1.0 / math.sqrt(128), w_std=1.0 / 8, materialise_logits=False),
-    "v41_packed": _w("v41_packed", B=1, S=8192, H=64, D=128, Skv=8192, ratio=4,
+    "v41_packed": _w("v41_packed", B=1, S=8192, H=64, D=128, Skv=8192, ratio=4, topk=512,
                      qk_std=1.0 / math.sqrt(128), w_std=1.0 / 8, query_offset=24576,
                      doc_min=512, doc_max=4096, kind="v41"),
     "bwd": _w("bwd", B=1, S=8192, H=64, D=128, Skv=2048, ratio=4, topk=1024,
