@@ -388,16 +388,19 @@ def side_workloads(lidx, pk):
     fn = lambda: lidx.lidx_indexer_bwd(q, k, w, idx, grad, wl.ratio, out=outs, workspace=ws)
     for _ in range(2):
         fn()
-    ms = time_steps(fn, 3, stream)
+    ms = time_steps(fn, 10, stream)
     nsel = int((idx >= 0).sum().item())
     fl = nsel * 6.0 * wl.H * wl.D
     out["bwd"] = {"ms": ms, "selected_pairs": nsel, "tflops": fl / ms / 1e9,
-                  "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"], "kernel": BWD_KERNEL}
+                  "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"], "kernel": BWD_KERNEL,
+                  "launches": 4, "algorithmic": "6*H*D FLOP per selected pair",
+                  "workspace_bytes": wsb}
     del q, k, w, idx, grad, outs, ws
     return out
 
 
-BWD_KERNEL = "bwd_rows_mma_kernel<64> (warp-level tf32 MMA)"
+BWD_KERNEL = ("bwd_scatter_kernel + bwd_tile_kernel<64,0> (dq, dw) + bwd_tile_kernel<64,1> (dk partials) "
+              "+ bwd_reduce_kernel; tcgen05, P as bf16 hi+lo from TMEM")
 
 
 def run_gpu(args, wl, world, rank, local):

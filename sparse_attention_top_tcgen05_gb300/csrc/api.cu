@@ -515,7 +515,7 @@ static int indexer_bwd_impl(const void* q, const void* k, const float* w, const 
     if (!aligned16(q) || !aligned16(k) || !aligned16(w) || !aligned16(dq) || !aligned16(dk) ||
         !aligned16(dw) || !aligned16(idx) || !aligned16(grad_scores))
         return LIDX_ERR_ALIGN;
-    if (grad_dtype != 0) return LIDX_ERR_UNSUPPORTED;
+    if (Skv > kTopkMaxKeys) return LIDX_ERR_UNSUPPORTED;
     const int sms = device_sms(true);
     if (sms <= 0) return LIDX_ERR_NO_DEVICE;
     const size_t need = bwd_workspace_bytes(B, S, Skv, H, D, topk, sms);

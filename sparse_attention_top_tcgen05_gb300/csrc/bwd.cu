@@ -3,424 +3,847 @@
 // grad_indices); grad_indices carries no gradient).
 //
 // For query row (b,s) and selected slot j with key t = idx[j] inside the row's
-// causal range and g = grad[j], with x_h = q[s,b,h,:] . k[t,b,:]:
+// visible range and g = grad[j], with x_h = q[s,b,h,:] . k[t,b,:]:
 //     dw[s,b,h]   += g * act(x_h)
-//     c_h          = g * w[s,b,h] * act'(x_h)          (ReLU'(0) = 0)
-//     dq[s,b,h,:] += c_h * k[t,b,:]
-//     dk[t,b,:]   += sum_h c_h * q[s,b,h,:]
+//     P_h          = g * w[s,b,h] * act'(x_h)          (ReLU'(0) = 0)
+//     dq[s,b,h,:] += P_h * k[t,b,:]
+//     dk[t,b,:]   += sum_h P_h * q[s,b,h,:]
 //
-// One CTA per query row.  The row's queries stay in shared memory; its
-// selected keys are gathered in chunks of J.  Per chunk three small
-// contractions run, on warp-level tf32 MMA tiles when H is a multiple of 16
-// (bwd_rows_mma_kernel) and on the CUDA cores with register tiles of four
-// otherwise (bwd_rows_kernel):
-//     X [H x J]  = Q [H x D] . Kc^T        (then dw and C = g*w*act'(x))
-//     dq[H x D] += C [H x J] . Kc [J x D]  (accumulated in registers)
-//     dKc[J x D] = C^T [J x H] . Q [H x D] (scatter-added to dk)
-// dq and dw are written once per row; dk is cleared by the caller-side
-// launcher and accumulated with atomics (order-dependent in the last bits).
+// Four launches, all on the caller's stream:
+//   1. bwd_scatter_kernel: the selected grads become a dense G[b,s,t] (0 where
+//      nothing is selected; slots outside the row's range are dropped).
+//   2. bwd_tile_kernel<H, 0>, query-major.  A persistent CTA takes tiles of
+//      128 (query, head) rows and sweeps their visible keys 128 at a time:
+//        X = Q K^T                 tcgen05, bf16 -> fp32 into TMEM
+//        P = G w act'(X), dw += G act(X)   epilogue warps, one TMEM lane each;
+//            P goes back into the same TMEM columns as bf16 hi + lo halves
+//        dq += P_hi K + P_lo K     tcgen05 with A read from TMEM, K as an
+//                                  MN-major operand of the same shared tile
+//      dq and dw are written once per row tile.
+//   3. bwd_tile_kernel<H, 1>, key-major: the same pipeline with the roles of
+//      the operands swapped -- a tile of 128 keys sweeps a chunk of query tiles
+//      (128 (query, head) columns each), X^T = K Q^T, P^T, dk += P^T Q -- and
+//      writes one partial dk per (key tile, chunk).
+//   4. bwd_reduce_kernel: dk = each key tile's partials summed in chunk order.
+// No atomic operation touches dq, dk or dw: the results are deterministic.
+//
+// P is split into two bf16 halves (hi = bf16(P), lo = bf16(P - hi)) because the
+// tensor cores multiply bf16 by bf16; together they carry about 16 bits of P.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <string.h>
 
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace lidx {
 
-constexpr int kBwdThreads = 256;
-constexpr int kBwdJ = 64;  // selected keys per chunk
+constexpr int kBT = 128;                           // rows of a tile; columns of X
+constexpr int kBStages = 3;                        // streamed-tile ring
+constexpr int kBRegions = 3;                       // X/P regions in TMEM, 128 columns each
+constexpr int kBEpiWarps = 8;                      // two per TMEM lane quadrant
+constexpr int kBThreads = 64 + 32 * kBEpiWarps;
+constexpr int kBMaxKeyTiles = 512;                 // Skv <= 65536
+constexpr uint32_t kBTileBytes = kBT * 128;        // one 64-wide block of a 128-row tile
 
-__device__ __forceinline__ float bf16_to_f(uint16_t v) { return __uint_as_float((uint32_t)v << 16); }
+struct BwdParams {
+    int B, S, Skv, H, D, Dp, ratio, act, grad_dtype;
+    const int32_t* ks;  // nullable with ke: causal ranges from ratio
+    const int32_t* ke;
+    const float* w;     // [S,B,H]
+    const float* G;     // [B,S,Skv_pad] dense selected grads
+    int Skv_pad;
+    void* dq;           // [S,B,H,D] fp32 or bf16
+    float* dw;          // [S,B,H]
+    float* part;        // [B*U][128][Dp] partial dk
+    int qtiles, ntk, QT, nkb;
+    int num_units;
+    int U, CH;          // key-major: units per batch, query tiles per chunk
+    uint64_t wait_ns;
+    int pre[kBMaxKeyTiles + 1];  // key-major: first unit of each key tile within a batch
+};
 
-template <int H>
-__global__ void __launch_bounds__(kBwdThreads)
-    bwd_rows_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
-                    const float* __restrict__ w, const int32_t* __restrict__ idx,
-                    const float* __restrict__ grad, int B, int S, int Skv, int D, int ratio,
-                    const int32_t* __restrict__ ksa, const int32_t* __restrict__ kea,
-                    int topk, int act, float* __restrict__ dq, float* __restrict__ dk,
-                    float* __restrict__ dw) {
-    extern __shared__ __align__(16) float sm[];
-    const int DP = D + 4;                      // padded row stride (keeps 16-byte alignment)
-    float* qs = sm;                            // [H][DP]
-    float* kc = qs + H * DP;                   // [J][DP]   gathered keys
-    float* kT = kc + kBwdJ * DP;               // [D][J+4]  the same keys transposed
-    float* cs = kT + D * (kBwdJ + 4);          // [H][J+4]  C = g*w*act'(x)
-    float* ws = cs + H * (kBwdJ + 4);          // [H]
-    float* dws = ws + H;                       // [H]
-    float* gs = dws + H;                       // [J]
-    int* ts = reinterpret_cast<int*>(gs + kBwdJ);  // [J]   key, or -1
-    const int tid = threadIdx.x;
-    const int D4 = D / 4;
-    constexpr int JP = kBwdJ + 4;
-    // fixed work split of the three contractions
-    const int nX = H * (kBwdJ / 4);            // groups (h, 4 keys)
-    const int nQ = H * D4;                     // groups (h, 4 dims)
-    const int nK = kBwdJ * D4;                 // groups (key, 4 dims)
-    constexpr int MAXQ = (H * 32 + kBwdThreads - 1) / kBwdThreads;  // D <= 128
+__device__ __forceinline__ void bwd_row_range(const BwdParams& p, int s, int& lo, int& hi) {
+    if (p.ks == nullptr) {
+        lo = 0;
+        const long long e = (long long)(s + 1) / p.ratio;
+        hi = (int)(e < p.Skv ? e : p.Skv);
+    } else {
+        lo = p.ks[s] > 0 ? p.ks[s] : 0;
+        hi = p.ke[s] < p.Skv ? p.ke[s] : p.Skv;
+        if (hi < lo) hi = lo;
+    }
+}
 
-    for (int r = blockIdx.x; r < B * S; r += gridDim.x) {
-        const int b = r / S, s = r % S;
-        int ks = 0, ke;
-        if (ksa) {
-            ks = ksa[s] > 0 ? ksa[s] : 0;
-            ke = kea[s] < Skv ? kea[s] : Skv;
+// Union [lo, hi) of the visible ranges of query tile qt's rows (empty: hi <= lo).
+__device__ __forceinline__ void qtile_range(const BwdParams& p, int qt, int& lo, int& hi) {
+    const int s0 = qt * p.QT, s1 = min(s0 + p.QT, p.S) - 1;
+    if (p.ks == nullptr) {
+        bwd_row_range(p, s1, lo, hi);
+        return;
+    }
+    lo = p.Skv;
+    hi = 0;
+    for (int s = s0; s <= s1; ++s) {
+        int a, e;
+        bwd_row_range(p, s, a, e);
+        if (e > a) {
+            lo = min(lo, a);
+            hi = max(hi, e);
+        }
+    }
+}
+
+struct BUnit {
+    int b, res;         // batch; resident tile (query tile for MODE 0, key tile for MODE 1)
+    int first, last;    // streamed tiles [first, last) (key tiles, or query tiles)
+};
+
+template <int MODE>
+__device__ __forceinline__ BUnit bwd_unit(const BwdParams& p, int u) {
+    BUnit un;
+    if constexpr (MODE == 0) {
+        un.res = p.qtiles - 1 - u / p.B;  // heaviest (latest) query tiles first
+        un.b = u % p.B;
+        int lo, hi;
+        qtile_range(p, un.res, lo, hi);
+        if (hi > lo) {
+            un.first = lo / kBT;
+            un.last = (hi + kBT - 1) / kBT;
         } else {
-            const long long ke_ll = (long long)(s + 1) / ratio;
-            ke = (int)(ke_ll < Skv ? ke_ll : Skv);
+            un.first = un.last = 0;
         }
-        __syncthreads();  // previous row done with shared memory
-        for (int e = tid; e < H * D; e += kBwdThreads) {
-            const int h = e / D, d = e % D;
-            qs[h * DP + d] = bf16_to_f(q[(((size_t)s * B + b) * H + h) * D + d]);
+    } else {
+        un.b = u / p.U;
+        const int r = u % p.U;
+        int a = 0, z = p.ntk - 1;  // last key tile whose first unit is <= r
+        while (a < z) {
+            const int mid = (a + z + 1) >> 1;
+            if (p.pre[mid] <= r)
+                a = mid;
+            else
+                z = mid - 1;
         }
-        for (int h = tid; h < H; h += kBwdThreads) {
-            ws[h] = w[((size_t)s * B + b) * H + h];
-            dws[h] = 0.f;
+        un.res = a;
+        int qlo = 0;
+        if (p.ks == nullptr) {  // the first query row that sees key a*128
+            const long long s_min = ((long long)a * kBT + 1) * p.ratio - 1;
+            qlo = (int)(s_min / p.QT);
         }
-        float accq[MAXQ][4];
-#pragma unroll
-        for (int i = 0; i < MAXQ; ++i)
-#pragma unroll
-            for (int c = 0; c < 4; ++c) accq[i][c] = 0.f;
+        un.first = qlo + (r - p.pre[a]) * p.CH;
+        un.last = min(un.first + p.CH, p.qtiles);
+    }
+    return un;
+}
 
-        const int32_t* irow = idx + (size_t)r * topk;
-        const float* grow = grad + (size_t)r * topk;
-        for (int j0 = 0; j0 < topk; j0 += kBwdJ) {
-            __syncthreads();  // previous chunk done with kc/kT/cs
-            for (int j = tid; j < kBwdJ; j += kBwdThreads) {
-                const int slot = j0 + j;
-                int t = slot < topk ? irow[slot] : -1;
-                if (t < ks || t >= ke) t = -1;  // padding or outside the causal range
-                ts[j] = t;
-                gs[j] = t >= 0 ? grow[slot] : 0.f;
-            }
-            __syncthreads();
-            for (int e = tid; e < kBwdJ * D; e += kBwdThreads) {
-                const int j = e / D, d = e % D;
-                const int t = ts[j];
-                const float v = t >= 0 ? bf16_to_f(k[((size_t)t * B + b) * D + d]) : 0.f;
-                kc[j * DP + d] = v;
-                kT[d * JP + j] = v;
-            }
-            __syncthreads();
-            // X and C: thread group (h, four keys)
-            for (int gi = tid; gi < nX; gi += kBwdThreads) {
-                const int h = gi / (kBwdJ / 4), j4 = (gi % (kBwdJ / 4)) * 4;
-                float x0 = 0.f, x1 = 0.f, x2 = 0.f, x3 = 0.f;
-                const float* qh = qs + h * DP;
-                for (int d = 0; d < D; ++d) {
-                    const float qv = qh[d];
-                    const float4 kv = *reinterpret_cast<const float4*>(kT + d * JP + j4);
-                    x0 = fmaf(qv, kv.x, x0);
-                    x1 = fmaf(qv, kv.y, x1);
-                    x2 = fmaf(qv, kv.z, x2);
-                    x3 = fmaf(qv, kv.w, x3);
-                }
-                const float xs[4] = {x0, x1, x2, x3};
-                float dwp = 0.f, cv[4];
+// Streamed tile x of unit un has work.
+template <int MODE>
+__device__ __forceinline__ bool bwd_active(const BwdParams& p, const BUnit& un, int x) {
+    if constexpr (MODE == 0) return true;
+    int lo, hi;
+    qtile_range(p, x, lo, hi);
+    return hi > lo && hi > un.res * kBT && lo < un.res * kBT + kBT;
+}
+
+template <int MODE>
+__device__ __forceinline__ int bwd_count(const BwdParams& p, const BUnit& un) {
+    if constexpr (MODE == 0) return un.last - un.first;
+    int n = 0;
+    for (int x = un.first; x < un.last; ++x) n += bwd_active<MODE>(p, un, x);
+    return n;
+}
+
+// i-th unit of this CTA in snake order, -1 to skip, -2 past the end
+__device__ __forceinline__ int bwd_unit_of(int i, int num_units) {
+    const int G = gridDim.x;
+    const int base = i * G;
+    if (base >= num_units) return -2;
+    const int u = base + ((i & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+    return u < num_units ? u : -1;
+}
+
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo_elem, float hi_elem) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi_elem), "f"(lo_elem));
+    return r;
+}
+
+// P of 32 columns -> packed bf16 hi and lo halves (element 2c in the low half).
+__device__ __forceinline__ void split_hi_lo(const float (&P)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float g = gs[j4 + c];
-                    const float x = xs[c];
-                    const float a = act == 0 ? fmaxf(x, 0.f) : x;
-                    const float da = act == 0 ? (x > 0.f ? 1.f : 0.f) : 1.f;
-                    dwp = fmaf(g, a, dwp);
-                    cv[c] = g * ws[h] * da;
+    for (int c = 0; c < 16; ++c) {
+        const uint32_t h2 = bf16x2_rn(P[2 * c], P[2 * c + 1]);
+        hi[c] = h2;
+        const float r0 = P[2 * c] - __uint_as_float(h2 << 16);
+        const float r1 = P[2 * c + 1] - __uint_as_float(h2 & 0xffff0000u);
+        lo[c] = bf16x2_rn(r0, r1);
+    }
+}
+
+template <int H, int MODE>
+__global__ void __launch_bounds__(kBThreads, 1)
+    bwd_tile_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ BwdParams p) {
+    constexpr int QT = kBT / H;  // queries per tile of 128 (query, head) rows
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int nkb = p.nkb;
+    const uint32_t tile_bytes = kBTileBytes * nkb;
+    uint8_t* sRes = smem;                          // [2] resident tiles
+    uint8_t* sStg = smem + 2 * tile_bytes;         // [kBStages] streamed tiles
+    float* sDw = (float*)(sStg + kBStages * tile_bytes);  // [2][128] dw partials of half 1
+    uint64_t* bars = (uint64_t*)(sDw + 2 * 2 * kBT);
+    uint64_t* res_full = bars;                     // [2]
+    uint64_t* res_empty = bars + 2;                // [2]
+    uint64_t* k_full = bars + 4;                   // [kBStages]
+    uint64_t* k_empty = k_full + kBStages;         // [kBStages]
+    uint64_t* x_full = k_empty + kBStages;         // [kBRegions]
+    uint64_t* p_full = x_full + kBRegions;         // [kBRegions]
+    uint64_t* r_free = p_full + kBRegions;         // [kBRegions]
+    uint64_t* acc_full = r_free + kBRegions;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* dw_full = acc_empty + 1;             // [2] column half 1 -> half 0
+    uint64_t* dw_empty = dw_full + 2;              // [2] half 0 -> half 1
+    uint32_t* tmem_slot = (uint32_t*)(dw_empty + 2);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(res_full + i, 1);
+            mbar_init(res_empty + i, 1);
+        }
+        for (int i = 0; i < kBStages; ++i) {
+            mbar_init(k_full + i, 1);
+            mbar_init(k_empty + i, 1);
+        }
+        for (int i = 0; i < kBRegions; ++i) {
+            mbar_init(x_full + i, 1);
+            mbar_init(p_full + i, kBEpiWarps);
+            mbar_init(r_free + i, 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, kBEpiWarps);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(dw_full + i, kBEpiWarps / 2);
+            mbar_init(dw_empty + i, kBEpiWarps / 2);
+        }
+        fence_mbar_init();
+        tma_prefetch_desc(&tmq);
+        tma_prefetch_desc(&tmk);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_slot, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint32_t acc_col = kBRegions * kBT;  // columns [384, 384 + Dp)
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int kcount = 0, ucount = 0;
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                const int u = bwd_unit_of(i, p.num_units);
+                if (u == -2) break;
+                if (u < 0) continue;
+                const BUnit un = bwd_unit<MODE>(p, u);
+                if (bwd_count<MODE>(p, un) == 0) continue;
+                const int ub = ucount & 1;
+                if (!(ok = mbar_wait(res_empty + ub, ((ucount >> 1) & 1) ^ 1, p.wait_ns))) break;
+                ++ucount;
+                mbar_arrive_expect_tx(res_full + ub, tile_bytes);
+                for (int kb = 0; kb < nkb; ++kb) {
+                    uint8_t* dst = sRes + ub * tile_bytes + kb * kBTileBytes;
+                    if constexpr (MODE == 0)  // q [S,B,H,D]: dims (D, H, B, S)
+                        tma_load_4d(dst, &tmq, res_full + ub, kb * 64, 0, un.b, un.res * QT);
+                    else  // k [Skv,B,D]: dims (D, B, Skv)
+                        tma_load_3d(dst, &tmk, res_full + ub, kb * 64, un.b, un.res * kBT);
                 }
-                *reinterpret_cast<float4*>(cs + h * JP + j4) = make_float4(cv[0], cv[1], cv[2], cv[3]);
-                atomicAdd(&dws[h], dwp);
-            }
-            __syncthreads();
-            // dq += C . Kc: thread group (h, four dims), kept in registers across chunks
-#pragma unroll
-            for (int i = 0; i < MAXQ; ++i) {
-                const int gi = tid + i * kBwdThreads;
-                if (gi < nQ) {
-                    const int h = gi / D4, d4 = (gi % D4) * 4;
-                    const float* ch = cs + h * JP;
-                    float a0 = accq[i][0], a1 = accq[i][1], a2 = accq[i][2], a3 = accq[i][3];
-                    for (int j = 0; j < kBwdJ; ++j) {
-                        const float cvj = ch[j];
-                        const float4 kv = *reinterpret_cast<const float4*>(kc + j * DP + d4);
-                        a0 = fmaf(cvj, kv.x, a0);
-                        a1 = fmaf(cvj, kv.y, a1);
-                        a2 = fmaf(cvj, kv.z, a2);
-                        a3 = fmaf(cvj, kv.w, a3);
+                for (int x = un.first; x < un.last && ok; ++x) {
+                    if (!bwd_active<MODE>(p, un, x)) continue;
+                    const int st = kcount % kBStages;
+                    if (!(ok = mbar_wait(k_empty + st, ((kcount / kBStages) & 1) ^ 1, p.wait_ns))) break;
+                    ++kcount;
+                    mbar_arrive_expect_tx(k_full + st, tile_bytes);
+                    for (int kb = 0; kb < nkb; ++kb) {
+                        uint8_t* dst = sStg + st * tile_bytes + kb * kBTileBytes;
+                        if constexpr (MODE == 0)
+                            tma_load_3d(dst, &tmk, k_full + st, kb * 64, un.b, x * kBT);
+                        else
+                            tma_load_4d(dst, &tmq, k_full + st, kb * 64, 0, un.b, x * QT);
                     }
-                    accq[i][0] = a0;
-                    accq[i][1] = a1;
-                    accq[i][2] = a2;
-                    accq[i][3] = a3;
                 }
-            }
-            // dk[t] += C^T . Q: thread group (key, four dims)
-            for (int gi = tid; gi < nK; gi += kBwdThreads) {
-                const int j = gi / D4, d4 = (gi % D4) * 4;
-                const int t = ts[j];
-                if (t < 0) continue;
-                float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-                for (int h = 0; h < H; ++h) {
-                    const float cvh = cs[h * JP + j];
-                    const float4 qv = *reinterpret_cast<const float4*>(qs + h * DP + d4);
-                    a0 = fmaf(cvh, qv.x, a0);
-                    a1 = fmaf(cvh, qv.y, a1);
-                    a2 = fmaf(cvh, qv.z, a2);
-                    a3 = fmaf(cvh, qv.w, a3);
-                }
-                float* o = dk + ((size_t)t * B + b) * D + d4;
-                atomicAdd(o + 0, a0);
-                atomicAdd(o + 1, a1);
-                atomicAdd(o + 2, a2);
-                atomicAdd(o + 3, a3);
             }
         }
-        // dq and dw of this row
+    } else if (warp == 1) {
+        // ------------------------------------------------------- MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc_x = idesc_bf16_f32(kBT, kBT);
+            const uint32_t idesc_2 = idesc_bf16_f32(kBT, (uint32_t)p.Dp) | (1u << 16);  // B MN-major
+            const int nk = p.Dp / 16;
+            // base descriptors of every buffer; a k-step adds its byte offset / 16 to the
+            // 14-bit start-address field (shared addresses stay below 256 KB: no carry)
+            uint64_t rd[2], sd[kBStages], md[kBStages];
 #pragma unroll
-        for (int i = 0; i < MAXQ; ++i) {
-            const int gi = tid + i * kBwdThreads;
-            if (gi < nQ) {
-                const int h = gi / D4, d4 = (gi % D4) * 4;
-                *reinterpret_cast<float4*>(dq + (((size_t)s * B + b) * H + h) * D + d4) =
-                    make_float4(accq[i][0], accq[i][1], accq[i][2], accq[i][3]);
+            for (int j = 0; j < 2; ++j) rd[j] = smem_desc_kmajor(smem_u32(sRes + j * tile_bytes), 128);
+#pragma unroll
+            for (int j = 0; j < kBStages; ++j) {
+                sd[j] = smem_desc_kmajor(smem_u32(sStg + j * tile_bytes), 128);
+                md[j] = smem_desc_mn_sw128(smem_u32(sStg + j * tile_bytes), kBTileBytes);
             }
+            auto koff16 = [](int k) {  // K-major k-step: 64-wide block, then 32 bytes per 16
+                return (uint64_t)((((k * 16) / 64) * kBTileBytes + ((k * 16) % 64) * 2) >> 4);
+            };
+            struct Pend {
+                int r, st, ub, tc, uc;
+                bool first, last;
+            } pend{};
+            bool have = false, ok = true;
+            auto second = [&](const Pend& t) -> bool {
+                if (!mbar_wait(p_full + t.r, (t.tc / kBRegions) & 1, p.wait_ns)) return false;
+                if (t.first && !mbar_wait(acc_empty, (t.uc & 1) ^ 1, p.wait_ns)) return false;
+                tc_fence_after();
+                const uint32_t a0 = tmem_base + t.r * kBT;
+                uint64_t b0 = md[0];
+#pragma unroll
+                for (int j = 1; j < kBStages; ++j) b0 = t.st == j ? md[j] : b0;
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t b = b0 + (uint64_t)((kk * 16 * 128) >> 4);  // 16 rows per step
+                    const uint32_t a = a0 + 32 * (kk >> 1) + 8 * (kk & 1);
+                    umma_f16_ts(tmem_base + acc_col, a, b, idesc_2, (t.first && kk == 0) ? 0u : 1u);
+                    umma_f16_ts(tmem_base + acc_col, a + 16, b, idesc_2, 1u);
+                }
+                umma_commit(r_free + t.r);
+                umma_commit(k_empty + t.st);
+                if (t.last) {
+                    umma_commit(acc_full);
+                    umma_commit(res_empty + t.ub);
+                }
+                return true;
+            };
+            int kcount = 0, tcount = 0, ucount = 0;
+            for (int i = 0; ok; ++i) {
+                const int u = bwd_unit_of(i, p.num_units);
+                if (u == -2) break;
+                if (u < 0) continue;
+                const BUnit un = bwd_unit<MODE>(p, u);
+                const int n = bwd_count<MODE>(p, un);
+                if (n == 0) continue;
+                const int ub = ucount & 1, uc = ucount;
+                if (!(ok = mbar_wait(res_full + ub, (ucount >> 1) & 1, p.wait_ns))) break;
+                ++ucount;
+                int idx = 0;
+                for (int x = un.first; x < un.last; ++x) {
+                    if (!bwd_active<MODE>(p, un, x)) continue;
+                    const int st = kcount % kBStages, r = tcount % kBRegions;
+                    if (!(ok = mbar_wait(k_full + st, (kcount / kBStages) & 1, p.wait_ns))) break;
+                    if (!(ok = mbar_wait(r_free + r, ((tcount / kBRegions) & 1) ^ 1, p.wait_ns))) break;
+                    tc_fence_after();
+                    const uint32_t d = tmem_base + r * kBT;
+                    const uint64_t a0 = ub == 1 ? rd[1] : rd[0];
+                    uint64_t b0 = sd[0];
+#pragma unroll
+                    for (int j = 1; j < kBStages; ++j) b0 = st == j ? sd[j] : b0;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        if (k < nk) umma_f16(d, a0 + koff16(k), b0 + koff16(k), idesc_x, k > 0 ? 1u : 0u);
+                    umma_commit(x_full + r);
+                    if (have && !(ok = second(pend))) break;
+                    pend = Pend{r, st, ub, tcount, uc, idx == 0, idx == n - 1};
+                    have = true;
+                    ++kcount;
+                    ++tcount;
+                    ++idx;
+                }
+            }
+            if (ok && have) second(pend);
         }
-        __syncthreads();
-        for (int h = tid; h < H; h += kBwdThreads) dw[((size_t)s * B + b) * H + h] = dws[h];
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int quad = warp & 3;           // TMEM lane quadrant this warp may read
+        const int half = (warp - 2) >> 2;    // columns [64*half, 64*half + 64)
+        const int row = quad * 32 + lane;    // TMEM lane = row of the resident tile
+        const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
+        int tcount = 0, ucount = 0, done_units = 0;
+        bool ok = true;
+        for (int i = 0; ok; ++i) {
+            const int u = bwd_unit_of(i, p.num_units);
+            if (u == -2) break;
+            if (u < 0) continue;
+            const BUnit un = bwd_unit<MODE>(p, u);
+            const int n = bwd_count<MODE>(p, un);
+            // this thread's output row
+            int s = 0, h = 0, t = 0;
+            bool rvalid;
+            if constexpr (MODE == 0) {
+                s = un.res * QT + row / H;
+                h = row % H;
+                rvalid = s < p.S;
+            } else {
+                t = un.res * kBT + row;
+                rvalid = true;  // partial rows past Skv are written and never read
+            }
+            const float wv = (MODE == 0 && rvalid) ? p.w[((size_t)s * p.B + un.b) * H + h] : 0.f;
+            float dw_acc = 0.f;
+            if (n > 0) {
+                for (int x = un.first; x < un.last; ++x) {
+                    if (!bwd_active<MODE>(p, un, x)) continue;
+                    const int r = tcount % kBRegions;
+                    if (!(ok = mbar_wait(x_full + r, (tcount / kBRegions) & 1, p.wait_ns))) break;
+                    ++tcount;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c = 2 * half; c < 2 * half + 2; ++c) {
+                        uint32_t xr[32];
+                        tmem_ld32(lane_addr + r * kBT + 32 * c, xr);
+                        float P[32];
+                        if constexpr (MODE == 0) {
+                            // columns = keys x*128 + 32c + i of this thread's query row
+                            float g[32];
+                            if (rvalid) {
+                                const float4* g4 = reinterpret_cast<const float4*>(
+                                    p.G + ((size_t)un.b * p.S + s) * p.Skv_pad + (size_t)x * kBT + 32 * c);
+#pragma unroll
+                                for (int v = 0; v < 8; ++v) {
+                                    const float4 q4 = g4[v];
+                                    g[4 * v] = q4.x;
+                                    g[4 * v + 1] = q4.y;
+                                    g[4 * v + 2] = q4.z;
+                                    g[4 * v + 3] = q4.w;
+                                }
+                            } else {
+#pragma unroll
+                                for (int v = 0; v < 32; ++v) g[v] = 0.f;
+                            }
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int v = 0; v < 32; ++v) {
+                                const float xv = __uint_as_float(xr[v]);
+                                if (p.act == 0) {
+                                    dw_acc = fmaf(g[v], fmaxf(xv, 0.f), dw_acc);
+                                    P[v] = xv > 0.f ? g[v] * wv : 0.f;
+                                } else {
+                                    dw_acc = fmaf(g[v], xv, dw_acc);
+                                    P[v] = g[v] * wv;
+                                }
+                            }
+                        } else {
+                            // columns = (query, head) 32c + i of query tile x; this thread's key t
+                            float gw[32];
+                            if constexpr (H >= 32) {
+                                // one query per chunk: one grad, 32 consecutive weights
+                                const int sq = x * QT + (32 * c) / H;
+                                if (sq < p.S) {
+                                    const float g = p.G[((size_t)un.b * p.S + sq) * p.Skv_pad + t];
+                                    const float4* w4 = reinterpret_cast<const float4*>(
+                                        p.w + ((size_t)sq * p.B + un.b) * H + (32 * c) % H);
+#pragma unroll
+                                    for (int v = 0; v < 8; ++v) {
+                                        const float4 q4 = w4[v];
+                                        gw[4 * v] = g * q4.x;
+                                        gw[4 * v + 1] = g * q4.y;
+                                        gw[4 * v + 2] = g * q4.z;
+                                        gw[4 * v + 3] = g * q4.w;
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int v = 0; v < 32; ++v) gw[v] = 0.f;
+                                }
+                            } else {
+#pragma unroll
+                                for (int v = 0; v < 32; ++v) {
+                                    const int col = 32 * c + v;
+                                    const int sq = x * QT + col / H, hq = col % H;
+                                    gw[v] = sq < p.S ? p.G[((size_t)un.b * p.S + sq) * p.Skv_pad + t] *
+                                                           p.w[((size_t)sq * p.B + un.b) * H + hq]
+                                                     : 0.f;
+                                }
+                            }
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int v = 0; v < 32; ++v) {
+                                const float xv = __uint_as_float(xr[v]);
+                                P[v] = (p.act == 0) ? (xv > 0.f ? gw[v] : 0.f) : gw[v];
+                            }
+                        }
+                        uint32_t hi[16], lo[16];
+                        split_hi_lo(P, hi, lo);
+                        tmem_st16(lane_addr + r * kBT + 32 * c, hi);
+                        tmem_st16(lane_addr + r * kBT + 32 * c + 16, lo);
+                    }
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(p_full + r);
+                }
+                if (!ok) break;
+            }
+            // outputs of the unit: 64 columns of the accumulator per thread
+            float out[64];
+            if (n > 0) {
+                if (!(ok = mbar_wait(acc_full, ucount & 1, p.wait_ns))) break;
+                ++ucount;
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ar[32];
+                    if (64 * half + 32 * c < p.Dp) {
+                        tmem_ld32(lane_addr + acc_col + 64 * half + 32 * c, ar);
+                        tmem_ld_wait();
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < 32; ++v) ar[v] = 0u;
+                    }
+#pragma unroll
+                    for (int v = 0; v < 32; ++v) out[32 * c + v] = __uint_as_float(ar[v]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            } else {
+#pragma unroll
+                for (int v = 0; v < 64; ++v) out[v] = 0.f;
+            }
+            const int d0 = 64 * half;
+            const int dn = min(64, p.D - d0);  // valid output columns of this half
+            if constexpr (MODE == 0) {
+                if (rvalid && dn > 0) {
+                    const size_t o = (((size_t)s * p.B + un.b) * H + h) * p.D + d0;
+                    if (p.grad_dtype == 0) {
+                        float* dst = (float*)p.dq + o;
+                        if (dn == 64 && (p.D & 3) == 0) {
+#pragma unroll
+                            for (int v = 0; v < 16; ++v)
+                                reinterpret_cast<float4*>(dst)[v] =
+                                    make_float4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
+                        } else {
+                            for (int v = 0; v < dn; ++v) dst[v] = out[v];
+                        }
+                    } else {
+                        uint16_t* dst = (uint16_t*)p.dq + o;
+                        for (int v = 0; v < dn; v += 2) {
+                            const uint32_t pr = bf16x2_rn(out[v], v + 1 < dn ? out[v + 1] : 0.f);
+                            dst[v] = (uint16_t)(pr & 0xffffu);
+                            if (v + 1 < dn) dst[v + 1] = (uint16_t)(pr >> 16);
+                        }
+                    }
+                }
+                // dw: the two column halves' partial sums, added in a fixed order;
+                // half 1 hands its partial to half 0 through a double buffer
+                const int db = done_units & 1;
+                const uint32_t dph = (done_units >> 1) & 1;
+                float* dwb = sDw + db * kBT;
+                if (half == 1) {
+                    if (!(ok = mbar_wait(dw_empty + db, dph ^ 1, p.wait_ns))) break;
+                    dwb[row] = dw_acc;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dw_full + db);
+                } else {
+                    if (!(ok = mbar_wait(dw_full + db, dph, p.wait_ns))) break;
+                    const float other = dwb[row];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(dw_empty + db);
+                    if (rvalid) p.dw[((size_t)s * p.B + un.b) * H + h] = dw_acc + other;
+                }
+            } else {
+                if (dn > 0) {
+                    float* dst = p.part + ((size_t)u * kBT + row) * p.Dp + d0;
+#pragma unroll
+                    for (int v = 0; v < 16; ++v)
+                        if (4 * v < p.Dp - d0)
+                            reinterpret_cast<float4*>(dst)[v] =
+                                make_float4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
+                }
+            }
+            ++done_units;
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, 512);
     }
 }
 
-// Same computation as bwd_rows_kernel with the three contractions on warp-level
-// tf32 MMA tiles (m16n8k8).  q and k are exact in tf32 (bf16 values); the
-// accumulators are fp32; C = g*w*act'(x) is rounded to tf32 (nearest).  Fragment
-// coordinates: g = lane/4, c = lane%4; A rows g and g+8, columns c and c+4;
-// B column g, rows c and c+4; D rows g and g+8, columns 2c and 2c+1.
-template <int H>
-__global__ void __launch_bounds__(kBwdThreads)
-    bwd_rows_mma_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
-                        const float* __restrict__ w, const int32_t* __restrict__ idx,
-                        const float* __restrict__ grad, int B, int S, int Skv, int D, int ratio,
-                        const int32_t* __restrict__ ksa, const int32_t* __restrict__ kea,
-                        int topk, int act, float* __restrict__ dq, float* __restrict__ dk,
-                        float* __restrict__ dw) {
-    static_assert(H % 16 == 0, "H must be a multiple of 16");
-    extern __shared__ __align__(16) float sm[];
-    const int DP = D + 4;
-    constexpr int JP = kBwdJ + 4;
-    float* qs = sm;                      // [H][DP]
-    float* kc = qs + H * DP;             // [J][DP]
-    float* cs = kc + kBwdJ * DP;         // [H][JP]  C as tf32
-    float* ws = cs + H * JP;             // [H]
-    float* dws = ws + H;                 // [H]
-    float* gs = dws + H;                 // [J]
-    int* ts = reinterpret_cast<int*>(gs + kBwdJ);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, c4 = lane & 3;
-    constexpr int NWARP = kBwdThreads / 32;
-    constexpr int MT = H / 16;
-    const int NTD = D / 8;
-    constexpr int QT_MAX = (MT * 16 + NWARP - 1) / NWARP;  // dq tiles per warp at D = 128
-    auto u32 = [](float x) { return __float_as_uint(x); };
+// Dense selected grads: G[b,s,t] = sum of grad[b,s,j] over slots j with
+// idx[b,s,j] = t inside the row's visible range; 0 elsewhere.  One CTA per row
+// at a time; the row is built in shared memory when it fits.
+constexpr int kScatterThreads = 256;
 
+__global__ void __launch_bounds__(kScatterThreads)
+    bwd_scatter_kernel(const int32_t* __restrict__ idx, const float* __restrict__ grad, int B, int S,
+                       int Skv, int Skv_pad, int ratio, const int32_t* __restrict__ ksa,
+                       const int32_t* __restrict__ kea, int topk, float* __restrict__ G, int in_smem) {
+    extern __shared__ __align__(16) float srow[];
+    const int tid = threadIdx.x;
     for (int r = blockIdx.x; r < B * S; r += gridDim.x) {
-        const int b = r / S, s = r % S;
-        int ks = 0, ke;
-        if (ksa) {
-            ks = ksa[s] > 0 ? ksa[s] : 0;
-            ke = kea[s] < Skv ? kea[s] : Skv;
+        const int s = r % S;
+        int lo, hi;
+        if (ksa == nullptr) {
+            lo = 0;
+            const long long e = (long long)(s + 1) / ratio;
+            hi = (int)(e < Skv ? e : Skv);
         } else {
-            const long long ke_ll = (long long)(s + 1) / ratio;
-            ke = (int)(ke_ll < Skv ? ke_ll : Skv);
+            lo = ksa[s] > 0 ? ksa[s] : 0;
+            hi = kea[s] < Skv ? kea[s] : Skv;
         }
+        float* grow = G + (size_t)r * Skv_pad;
+        float* dst = in_smem ? srow : grow;
+        __syncthreads();  // the previous row is written out
+        for (int t = tid * 4; t < Skv_pad; t += kScatterThreads * 4)
+            *reinterpret_cast<float4*>(dst + t) = make_float4(0.f, 0.f, 0.f, 0.f);
         __syncthreads();
-        for (int e = tid; e < H * D; e += kBwdThreads) {
-            const int h = e / D, d = e % D;
-            qs[h * DP + d] = bf16_to_f(q[(((size_t)s * B + b) * H + h) * D + d]);
-        }
-        for (int h = tid; h < H; h += kBwdThreads) {
-            ws[h] = w[((size_t)s * B + b) * H + h];
-            dws[h] = 0.f;
-        }
-        float accq[QT_MAX][4];
-#pragma unroll
-        for (int i = 0; i < QT_MAX; ++i)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) accq[i][e] = 0.f;
-
         const int32_t* irow = idx + (size_t)r * topk;
-        const float* grow = grad + (size_t)r * topk;
-        for (int j0 = 0; j0 < topk; j0 += kBwdJ) {
-            __syncthreads();
-            for (int j = tid; j < kBwdJ; j += kBwdThreads) {
-                const int slot = j0 + j;
-                int t = slot < topk ? irow[slot] : -1;
-                if (t < ks || t >= ke) t = -1;
-                ts[j] = t;
-                gs[j] = t >= 0 ? grow[slot] : 0.f;
-            }
-            __syncthreads();
-            for (int e = tid; e < kBwdJ * D; e += kBwdThreads) {
-                const int j = e / D, d = e % D;
-                const int t = ts[j];
-                kc[j * DP + d] = t >= 0 ? bf16_to_f(k[((size_t)t * B + b) * D + d]) : 0.f;
-            }
-            __syncthreads();
-            // X = Q . Kc^T  [H x J]; then C and dw
-            for (int tt = warp; tt < MT * (kBwdJ / 8); tt += NWARP) {
-                const int mt = tt / (kBwdJ / 8), nt = tt % (kBwdJ / 8);
-                float x[4] = {0.f, 0.f, 0.f, 0.f};
-                const float* qa = qs + (mt * 16 + g) * DP + c4;
-                const float* kb = kc + (nt * 8 + g) * DP + c4;
-                for (int kk = 0; kk < D; kk += 8)
-                    mma_tf32(x, u32(qa[kk]), u32(qa[8 * DP + kk]), u32(qa[kk + 4]), u32(qa[8 * DP + kk + 4]),
-                             u32(kb[kk]), u32(kb[kk + 4]));
-                float dwp[2] = {0.f, 0.f};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int h = mt * 16 + g + (e >> 1) * 8, j = nt * 8 + 2 * c4 + (e & 1);
-                    const float xv = x[e], gv = gs[j];
-                    const float a = act == 0 ? fmaxf(xv, 0.f) : xv;
-                    const float da = act == 0 ? (xv > 0.f ? 1.f : 0.f) : 1.f;
-                    dwp[e >> 1] = fmaf(gv, a, dwp[e >> 1]);
-                    cs[h * JP + j] = __uint_as_float(tf32_round(gv * ws[h] * da));
-                }
-#pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    dwp[u] += __shfl_xor_sync(0xffffffffu, dwp[u], 1);
-                    dwp[u] += __shfl_xor_sync(0xffffffffu, dwp[u], 2);
-                }
-                if (c4 == 0) {
-                    atomicAdd(&dws[mt * 16 + g], dwp[0]);
-                    atomicAdd(&dws[mt * 16 + g + 8], dwp[1]);
-                }
-            }
-            __syncthreads();
-            // dq += C . Kc  [H x D], tiles kept in registers across chunks
-#pragma unroll
-            for (int i = 0; i < QT_MAX; ++i) {
-                const int tt = warp + i * NWARP;
-                if (tt < MT * NTD) {
-                    const int mt = tt / NTD, nt = tt % NTD;
-                    const float* ca = cs + (mt * 16 + g) * JP + c4;
-                    const float* kb = kc + c4 * DP + nt * 8 + g;
-#pragma unroll
-                    for (int kk = 0; kk < kBwdJ; kk += 8)
-                        mma_tf32(accq[i], u32(ca[kk]), u32(ca[8 * JP + kk]), u32(ca[kk + 4]),
-                                 u32(ca[8 * JP + kk + 4]), u32(kb[kk * DP]), u32(kb[(kk + 4) * DP]));
-                }
-            }
-            // dKc = C^T . Q  [J x D], scatter-added to dk
-            for (int tt = warp; tt < (kBwdJ / 16) * NTD; tt += NWARP) {
-                const int mt = tt / NTD, nt = tt % NTD;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                const float* ca = cs + c4 * JP + mt * 16 + g;  // A[j][h] = C[h][j]
-                const float* qb = qs + c4 * DP + nt * 8 + g;
-#pragma unroll
-                for (int kk = 0; kk < H; kk += 8)
-                    mma_tf32(acc, u32(ca[kk * JP]), u32(ca[kk * JP + 8]), u32(ca[(kk + 4) * JP]),
-                             u32(ca[(kk + 4) * JP + 8]), u32(qb[kk * DP]), u32(qb[(kk + 4) * DP]));
-                // Lanes c4 and c4^1 swap halves so that each holds four consecutive d of
-                // one key (even c4: key row g, odd c4: key row g + 8), then one 16-byte
-                // vector reduction per lane instead of four scalar ones.
-                const bool odd = (c4 & 1) != 0;
-                const float s0 = __shfl_xor_sync(0xffffffffu, odd ? acc[0] : acc[2], 1);
-                const float s1 = __shfl_xor_sync(0xffffffffu, odd ? acc[1] : acc[3], 1);
-                const int j = mt * 16 + g + (odd ? 8 : 0);
-                const int d0 = nt * 8 + 2 * (c4 & 2);
-                const int t = ts[j];
-                if (t >= 0) {
-                    const float4 v = odd ? make_float4(s0, s1, acc[2], acc[3])
-                                         : make_float4(acc[0], acc[1], s0, s1);
-                    atomicAdd(reinterpret_cast<float4*>(dk + ((size_t)t * B + b) * D + d0), v);
-                }
-            }
+        const float* gr = grad + (size_t)r * topk;
+        for (int j = tid; j < topk; j += kScatterThreads) {
+            const int t = irow[j];
+            if (t >= lo && t < hi) atomicAdd(dst + t, gr[j]);
         }
-#pragma unroll
-        for (int i = 0; i < QT_MAX; ++i) {
-            const int tt = warp + i * NWARP;
-            if (tt < MT * NTD) {
-                const int mt = tt / NTD, nt = tt % NTD;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int h = mt * 16 + g + (e >> 1) * 8, d = nt * 8 + 2 * c4 + (e & 1);
-                    dq[(((size_t)s * B + b) * H + h) * D + d] = accq[i][e];
-                }
-            }
+        if (in_smem) {
+            __syncthreads();
+            for (int t = tid * 4; t < Skv_pad; t += kScatterThreads * 4)
+                *reinterpret_cast<float4*>(grow + t) = *reinterpret_cast<const float4*>(srow + t);
         }
-        __syncthreads();
-        for (int h = tid; h < H; h += kBwdThreads) dw[((size_t)s * B + b) * H + h] = dws[h];
     }
 }
 
-static size_t bwd_mma_smem(int H, int D) {
-    const int DP = D + 4, JP = kBwdJ + 4;
-    return sizeof(float) * ((size_t)H * DP + (size_t)kBwdJ * DP + (size_t)H * JP + 2 * (size_t)H + kBwdJ) +
-           sizeof(int) * kBwdJ;
+// First partial-dk unit of each key tile within a batch (table size ntk + 1).
+struct UnitTable {
+    int pre[kBMaxKeyTiles + 1];
+};
+
+// dk[t,b,:] = sum over the key tile's chunks c of part[unit(b, t/128, c)][t%128][:],
+// in chunk order.
+__global__ void bwd_reduce_kernel(const float* __restrict__ part, int B, int Skv, int D, int Dp, int U,
+                                  const __grid_constant__ UnitTable tab, int grad_dtype, void* dk) {
+    const int D4 = D / 4;
+    const int64_t n = (int64_t)B * Skv * D4;
+    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
+         e += (int64_t)gridDim.x * blockDim.x) {
+        const int d4 = (int)(e % D4) * 4;
+        const int64_t bt = e / D4;
+        const int t = (int)(bt % Skv), b = (int)(bt / Skv);
+        const int kt = t / kBT, tl = t % kBT;
+        const int u0 = b * U + tab.pre[kt], u1 = b * U + tab.pre[kt + 1];
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = u0; u < u1; ++u) {
+            const float4 v = *reinterpret_cast<const float4*>(part + ((size_t)u * kBT + tl) * Dp + d4);
+            acc.x += v.x;
+            acc.y += v.y;
+            acc.z += v.z;
+            acc.w += v.w;
+        }
+        const size_t o = ((size_t)t * B + b) * D + d4;
+        if (grad_dtype == 0) {
+            *reinterpret_cast<float4*>((float*)dk + o) = acc;
+        } else {
+            const uint32_t lo = bf16x2_rn(acc.x, acc.y), hi = bf16x2_rn(acc.z, acc.w);
+            *reinterpret_cast<uint2*>((uint16_t*)dk + o) = make_uint2(lo, hi);
+        }
+    }
 }
 
-template <int H>
-static cudaError_t bwd_mma_h(const BwdLaunch& a) {
-    const size_t smem = bwd_mma_smem(H, a.D);
-    auto kern = bwd_rows_mma_kernel<H>;
-    cudaError_t e = set_smem_attr((const void*)kern, (int)smem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBwdThreads, smem);
-    if (per_sm < 1) per_sm = 1;
-    int64_t grid = (int64_t)a.num_sms * per_sm;
-    const int64_t rows = (int64_t)a.B * a.S;
-    if (grid > rows) grid = rows;
-    kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(
-        (const uint16_t*)a.q, (const uint16_t*)a.k, a.w, a.idx, a.grad, a.B, a.S, a.Skv, a.D, a.ratio,
-        a.ks, a.ke, a.topk, a.act, (float*)a.dq, (float*)a.dk, a.dw);
-    return cudaGetLastError();
-}
-
-static size_t bwd_smem(int H, int D) {
-    const int DP = D + 4, JP = kBwdJ + 4;
-    return sizeof(float) * ((size_t)H * DP + (size_t)kBwdJ * DP + (size_t)D * JP + (size_t)H * JP +
-                            2 * (size_t)H + kBwdJ) +
-           sizeof(int) * kBwdJ;
-}
-
-template <int H>
-static cudaError_t bwd_h(const BwdLaunch& a) {
-    const size_t smem = bwd_smem(H, a.D);
-    auto kern = bwd_rows_kernel<H>;
-    cudaError_t e = set_smem_attr((const void*)kern, (int)smem);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kBwdThreads, smem);
-    if (per_sm < 1) per_sm = 1;
-    int64_t grid = (int64_t)a.num_sms * per_sm;
-    const int64_t rows = (int64_t)a.B * a.S;
-    if (grid > rows) grid = rows;
-    kern<<<(unsigned)grid, kBwdThreads, smem, a.stream>>>(
-        (const uint16_t*)a.q, (const uint16_t*)a.k, a.w, a.idx, a.grad, a.B, a.S, a.Skv, a.D, a.ratio,
-        a.ks, a.ke, a.topk, a.act, (float*)a.dq, (float*)a.dk, a.dw);
-    return cudaGetLastError();
-}
-
+// ------------------------------------------------------------------- host
 LIDX_STATUS_READER(status_bwd)
 
-size_t bwd_workspace_bytes(int64_t, int64_t, int64_t, int, int, int, int) { return 0; }
+struct BwdPlan {
+    int Dp, QT, qtiles, ntk, Skv_pad, CH, U, nkb;
+    size_t g_bytes, part_bytes;
+    int pre[kBMaxKeyTiles + 1];
+};
+
+// Tiling of the backward; `causal` selects the first query tile of each key tile.
+static void bwd_plan(int64_t B, int64_t S, int64_t Skv, int H, int D, int ratio, bool causal, int sms,
+                     BwdPlan& pl) {
+    pl.Dp = (D + 63) / 64 * 64;
+    pl.nkb = pl.Dp / 64;
+    pl.QT = kBT / H;
+    pl.qtiles = (int)((S + pl.QT - 1) / pl.QT);
+    pl.ntk = (int)((Skv + kBT - 1) / kBT);
+    pl.Skv_pad = pl.ntk * kBT;
+    // query tiles per key tile, then chunks of CH so that there are about 4 units per SM
+    int64_t T = 0;
+    for (int kt = 0; kt < pl.ntk; ++kt) {
+        int qlo = 0;
+        if (causal) qlo = (int)((((int64_t)kt * kBT + 1) * ratio - 1) / pl.QT);
+        T += qlo < pl.qtiles ? pl.qtiles - qlo : 0;
+    }
+    T *= B;
+    const int64_t target = 4 * (int64_t)sms;
+    pl.CH = (int)((T + target - 1) / target);
+    if (pl.CH < 1) pl.CH = 1;
+    int U = 0;
+    for (int kt = 0; kt < pl.ntk; ++kt) {
+        pl.pre[kt] = U;
+        int qlo = 0;
+        if (causal) qlo = (int)((((int64_t)kt * kBT + 1) * ratio - 1) / pl.QT);
+        const int nq = qlo < pl.qtiles ? pl.qtiles - qlo : 0;
+        U += (nq + pl.CH - 1) / pl.CH;
+    }
+    pl.pre[pl.ntk] = U;
+    pl.U = U;
+    pl.g_bytes = ((size_t)B * S * pl.Skv_pad * 4 + 255) / 256 * 256;
+    pl.part_bytes = (size_t)B * U * kBT * pl.Dp * 4;
+}
+
+// Partial dk units per batch are at most T/CH + ntk <= 4*sms/B + ntk, whatever
+// the ranges, so this bound holds for causal and explicit-range calls alike.
+size_t bwd_workspace_bytes(int64_t B, int64_t S, int64_t Skv, int H, int D, int topk, int num_sms) {
+    (void)topk;
+    if (B <= 0 || S <= 0 || Skv <= 0 || H < 1 || H > 128) return 0;
+    const int64_t Dp = (D + 63) / 64 * 64;
+    const int64_t ntk = (Skv + kBT - 1) / kBT;
+    const size_t g = ((size_t)B * S * ntk * kBT * 4 + 255) / 256 * 256;
+    const size_t units = (size_t)4 * num_sms + (size_t)B * ntk;
+    return g + units * kBT * Dp * 4;
+}
+
+static int encode_bwd_maps(const BwdLaunch& a, CUtensorMap* mq, CUtensorMap* mk, int QT) {
+    const int H = a.H, D = a.D, B = a.B;
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    // q [S,B,H,D]: dims (D, H, B, S); a 128-row tile = QT queries x H heads
+    cuuint64_t qdim[4] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)B, (cuuint64_t)a.S};
+    cuuint64_t qstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2, (cuuint64_t)B * H * D * 2};
+    cuuint32_t qbox[4] = {64, (cuuint32_t)H, 1, (cuuint32_t)QT};
+    if (encode_tiled(mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void*)a.q, qdim, qstr, qbox, es,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return 1;
+    // k [Skv,B,D]: dims (D, B, Skv)
+    cuuint64_t kdim[3] = {(cuuint64_t)D, (cuuint64_t)B, (cuuint64_t)a.Skv};
+    cuuint64_t kstr[2] = {(cuuint64_t)D * 2, (cuuint64_t)B * D * 2};
+    cuuint32_t kbox[3] = {64, 1, (cuuint32_t)kBT};
+    if (encode_tiled(mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.k, kdim, kstr, kbox, es,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return 1;
+    return 0;
+}
+
+static size_t bwd_smem_bytes(int nkb) {
+    return 1024 + (size_t)(2 + kBStages) * kBTileBytes * nkb + 2 * 2 * kBT * 4 + 32 * 8 + 16;
+}
+
+template <int H>
+static cudaError_t bwd_tiles_h(const CUtensorMap& mq, const CUtensorMap& mk, const BwdParams& p0,
+                               const BwdLaunch& a) {
+    // at least 120 KB so that one CTA (and its 512 TMEM columns) owns each SM
+    int smem = (int)bwd_smem_bytes(p0.nkb);
+    if (smem < 120 * 1024) smem = 120 * 1024;
+    BwdParams p = p0;
+    // dq and dw, query-major
+    {
+        auto kern = bwd_tile_kernel<H, 0>;
+        cudaError_t e = set_smem_attr((const void*)kern, smem);
+        if (e != cudaSuccess) return e;
+        p.num_units = p.B * p.qtiles;
+        const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+        if (grid > 0) kern<<<grid, kBThreads, smem, a.stream>>>(mq, mk, p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // partial dk, key-major
+    {
+        auto kern = bwd_tile_kernel<H, 1>;
+        cudaError_t e = set_smem_attr((const void*)kern, smem);
+        if (e != cudaSuccess) return e;
+        p.num_units = p.B * p.U;
+        const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
+        if (grid > 0) kern<<<grid, kBThreads, smem, a.stream>>>(mq, mk, p);
+        return cudaGetLastError();
+    }
+}
 
 cudaError_t bwd_launch(const BwdLaunch& a) {
-    // dk is a sum over rows: clear it first (dq and dw are written whole)
-    cudaError_t e = cudaMemsetAsync(a.dk, 0, sizeof(float) * (size_t)a.Skv * a.B * a.D, a.stream);
-    if (e != cudaSuccess) return e;
-    if ((int64_t)a.B * a.S == 0) return cudaSuccess;
-    switch (a.H) {
-        case 1: return bwd_h<1>(a);
-        case 2: return bwd_h<2>(a);
-        case 4: return bwd_h<4>(a);
-        case 8: return bwd_h<8>(a);
-        case 16: return bwd_mma_h<16>(a);
-        case 32: return bwd_mma_h<32>(a);
-        case 64: return bwd_mma_h<64>(a);
-        case 128: return bwd_mma_h<128>(a);
-        default: return cudaErrorInvalidValue;
+    const int64_t rows = (int64_t)a.B * a.S;
+    const size_t es = a.grad_dtype ? 2 : 4;
+    if (a.Skv == 0) {  // nothing visible: every gradient is zero
+        cudaError_t e = cudaMemsetAsync(a.dq, 0, es * (size_t)rows * a.H * a.D, a.stream);
+        if (e != cudaSuccess) return e;
+        return cudaMemsetAsync(a.dw, 0, sizeof(float) * (size_t)rows * a.H, a.stream);
     }
+    if ((a.Skv + kBT - 1) / kBT > kBMaxKeyTiles || a.H < 1 || a.H > 128) return cudaErrorInvalidValue;
+    BwdPlan pl;
+    bwd_plan(a.B, a.S, a.Skv, a.H, a.D, a.ratio, a.ks == nullptr, a.num_sms, pl);
+    if (pl.g_bytes + pl.part_bytes > a.workspace_bytes) return cudaErrorInvalidValue;
+    float* G = (float*)a.workspace;
+    float* part = (float*)((uint8_t*)a.workspace + pl.g_bytes);
+
+    // 1. dense selected grads
+    {
+        const size_t row_bytes = (size_t)pl.Skv_pad * 4;
+        const int in_smem = row_bytes <= 64 * 1024;
+        const int smem = in_smem ? (int)row_bytes : 0;
+        if (in_smem) {
+            cudaError_t e = set_smem_attr((const void*)bwd_scatter_kernel, smem);
+            if (e != cudaSuccess) return e;
+        }
+        int64_t grid = (int64_t)a.num_sms * 4;
+        if (grid > rows) grid = rows;
+        bwd_scatter_kernel<<<(unsigned)grid, kScatterThreads, smem, a.stream>>>(
+            a.idx, a.grad, a.B, a.S, a.Skv, pl.Skv_pad, a.ratio, a.ks, a.ke, a.topk, G, in_smem);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    // 2, 3. tensor-core tiles
+    CUtensorMap mq, mk;
+    if (encode_bwd_maps(a, &mq, &mk, pl.QT)) return cudaErrorInvalidValue;
+    BwdParams p;
+    memset(&p, 0, sizeof p);
+    p.B = a.B;
+    p.S = a.S;
+    p.Skv = a.Skv;
+    p.H = a.H;
+    p.D = a.D;
+    p.Dp = pl.Dp;
+    p.nkb = pl.nkb;
+    p.ratio = a.ratio;
+    p.act = a.act;
+    p.grad_dtype = a.grad_dtype;
+    p.ks = a.ks;
+    p.ke = a.ke;
+    p.w = a.w;
+    p.G = G;
+    p.Skv_pad = pl.Skv_pad;
+    p.dq = a.dq;
+    p.dw = a.dw;
+    p.part = part;
+    p.qtiles = pl.qtiles;
+    p.ntk = pl.ntk;
+    p.QT = pl.QT;
+    p.U = pl.U;
+    p.CH = pl.CH;
+    p.wait_ns = wait_limit_ns();
+    memcpy(p.pre, pl.pre, sizeof(int) * (pl.ntk + 1));
+    cudaError_t e;
+    switch (a.H) {
+        case 1: e = bwd_tiles_h<1>(mq, mk, p, a); break;
+        case 2: e = bwd_tiles_h<2>(mq, mk, p, a); break;
+        case 4: e = bwd_tiles_h<4>(mq, mk, p, a); break;
+        case 8: e = bwd_tiles_h<8>(mq, mk, p, a); break;
+        case 16: e = bwd_tiles_h<16>(mq, mk, p, a); break;
+        case 32: e = bwd_tiles_h<32>(mq, mk, p, a); break;
+        case 64: e = bwd_tiles_h<64>(mq, mk, p, a); break;
+        case 128: e = bwd_tiles_h<128>(mq, mk, p, a); break;
+        default: e = cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+    // 4. fixed-order reduction of the partial dk
+    UnitTable tab;
+    memcpy(tab.pre, pl.pre, sizeof(int) * (pl.ntk + 1));
+    const int64_t n = (int64_t)a.B * a.Skv * (a.D / 4);
+    int64_t grid = (n + 255) / 256;
+    if (grid > (int64_t)a.num_sms * 8) grid = (int64_t)a.num_sms * 8;
+    bwd_reduce_kernel<<<(unsigned)grid, 256, 0, a.stream>>>(part, a.B, a.Skv, a.D, pl.Dp, pl.U, tab,
+                                                           a.grad_dtype, a.dk);
+    return cudaGetLastError();
 }
 
 }  // namespace lidx

@@ -2,7 +2,8 @@
 
 Tolerance per tensor: 1e-3 relative or 1e-3*max|ref| absolute, widened per
 element by the oracle's slack for pairs whose ReLU decision lies within fp32
-accumulation error."""
+accumulation error.  The backward uses no atomics on its outputs, so two runs
+must agree bit for bit; bf16 outputs are the fp32 results rounded once."""
 
 import numpy as np
 import pytest
@@ -58,6 +59,9 @@ def selection(B, S, Skv, ratio, topk, seed):
     (1, 257, 64, 128, 200, 1, 100),
     (3, 100, 128, 64, 30, 2, 40),     # topk > visible keys: padding slots
     (1, 129, 1, 16, 129, 1, 7),
+    (1, 200, 16, 64, 300, 2, 50),     # heads below 32: one grad per column in the key-major pass
+    (2, 150, 32, 128, 260, 1, 90),
+    (1, 700, 4, 48, 650, 1, 300),     # index_dim not a multiple of 64
 ])
 def test_random_selection(B, S, H, D, Skv, ratio, topk):
     g = np.random.default_rng(S + H)
@@ -93,3 +97,22 @@ def test_backward_workload_sampled_rows():
     keep[workloads.sample_rows(1, wl.S, 97, 11)] = True
     idx[:, ~keep] = -1
     run_case(q, k, w, idx, grad.numpy(), wl.ratio)
+
+
+def test_deterministic_and_bf16_outputs():
+    """Two runs give identical bits; grad_dtype bf16 returns the fp32 results
+    rounded to nearest-even once."""
+    wl = workloads.WORKLOADS["bwd"].with_(S=2048, Skv=512, topk=256)
+    ks, ke = oracle.causal_ranges(wl.S, wl.Skv, wl.ratio)
+    q, k, w, idx, grad = workloads.bwd_inputs(wl, ke - ks, 3)
+    args = [t.to(DEV) for t in (q, k, w, idx, grad)]
+    a = lidx.lidx_indexer_bwd(*args, wl.ratio)
+    b = lidx.lidx_indexer_bwd(*args, wl.ratio)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    c = lidx.lidx_indexer_bwd(*args, wl.ratio, grad_dtype=torch.bfloat16)
+    torch.cuda.synchronize()
+    assert lidx.lidx_device_status() == 0
+    assert c[0].dtype == torch.bfloat16 and c[1].dtype == torch.bfloat16
+    assert torch.equal(c[0], a[0].to(torch.bfloat16)) and torch.equal(c[1], a[1].to(torch.bfloat16))
+    assert torch.equal(c[2], a[2])
