@@ -42,9 +42,15 @@ namespace lidx {
 constexpr int kBT = 128;                           // rows of a tile; columns of X
 constexpr int kBStages = 3;                        // streamed-tile ring
 constexpr int kBRegions = 3;                       // X/P regions in TMEM, 128 columns each
-constexpr int kBEpiWarps = 8;                      // two per TMEM lane quadrant
+// The second product of a tile is issued after the X product of the next tile,
+// so the epilogue of one tile overlaps the X product of the next.  (Issuing two
+// X products ahead measured slower.)  Two resident tiles then suffice.
+constexpr int kBLookahead = 1;
+constexpr int kBRes = 2;
+constexpr int kBEpiWarps = 8;                      // two per TMEM lane quadrant, 64 columns each
 constexpr int kBThreads = 64 + 32 * kBEpiWarps;
 constexpr int kBMaxKeyTiles = 512;                 // Skv <= 65536
+constexpr int kBMaxChunks = 512;                   // chunks of query tiles (key-major)
 constexpr uint32_t kBTileBytes = kBT * 128;        // one 64-wide block of a 128-row tile
 
 struct BwdParams {
@@ -59,9 +65,9 @@ struct BwdParams {
     float* part;        // [B*U][128][Dp] partial dk
     int qtiles, ntk, QT, nkb;
     int num_units;
-    int U, CH;          // key-major: units per batch, query tiles per chunk
+    int U, CH, nchunks; // key-major: units per batch, query tiles per chunk, chunks
     uint64_t wait_ns;
-    int pre[kBMaxKeyTiles + 1];  // key-major: first unit of each key tile within a batch
+    int cpre[kBMaxChunks + 1];   // key-major: first unit of each chunk within a batch
 };
 
 __device__ __forceinline__ void bwd_row_range(const BwdParams& p, int s, int& lo, int& hi) {
@@ -95,6 +101,13 @@ __device__ __forceinline__ void qtile_range(const BwdParams& p, int qt, int& lo,
     }
 }
 
+// First query tile whose rows can see key tile kt (0 for explicit ranges).
+__host__ __device__ __forceinline__ int bwd_qlo(bool causal, int kt, int ratio, int QT) {
+    if (!causal) return 0;
+    const long long s_min = ((long long)kt * kBT + 1) * ratio - 1;  // first row seeing key kt*128
+    return (int)(s_min / QT);
+}
+
 struct BUnit {
     int b, res;         // batch; resident tile (query tile for MODE 0, key tile for MODE 1)
     int first, last;    // streamed tiles [first, last) (key tiles, or query tiles)
@@ -115,24 +128,21 @@ __device__ __forceinline__ BUnit bwd_unit(const BwdParams& p, int u) {
             un.first = un.last = 0;
         }
     } else {
+        // chunk-major: the units of one chunk (one per key tile) cover the same
+        // query tiles, so CTAs that run them at the same time share those tiles in L2
         un.b = u / p.U;
         const int r = u % p.U;
-        int a = 0, z = p.ntk - 1;  // last key tile whose first unit is <= r
+        int a = 0, z = p.nchunks - 1;  // last chunk whose first unit is <= r
         while (a < z) {
             const int mid = (a + z + 1) >> 1;
-            if (p.pre[mid] <= r)
+            if (p.cpre[mid] <= r)
                 a = mid;
             else
                 z = mid - 1;
         }
-        un.res = a;
-        int qlo = 0;
-        if (p.ks == nullptr) {  // the first query row that sees key a*128
-            const long long s_min = ((long long)a * kBT + 1) * p.ratio - 1;
-            qlo = (int)(s_min / p.QT);
-        }
-        un.first = qlo + (r - p.pre[a]) * p.CH;
-        un.last = min(un.first + p.CH, p.qtiles);
+        un.res = r - p.cpre[a];
+        un.first = max(a * p.CH, bwd_qlo(p.ks == nullptr, un.res, p.ratio, p.QT));
+        un.last = min((a + 1) * p.CH, p.qtiles);
     }
     return un;
 }
@@ -184,32 +194,39 @@ __device__ __forceinline__ void split_hi_lo(const float (&P)[32], uint32_t (&hi)
 template <int H, int MODE>
 __global__ void __launch_bounds__(kBThreads, 1)
     bwd_tile_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
+                    const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmw,
                     const __grid_constant__ BwdParams p) {
     constexpr int QT = kBT / H;  // queries per tile of 128 (query, head) rows
+    // With at least 8 heads, each stage also carries the tile's grads G [QT][128]
+    // (and, key-major, its weights [QT][H]), loaded by TMA with the operand.
+    constexpr bool kStaged = H >= 8;
+    constexpr uint32_t kGBytes = kStaged ? QT * kBT * 4 : 0;
+    constexpr uint32_t kWBytes = (kStaged && MODE == 1) ? QT * H * 4 : 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const int nkb = p.nkb;
     const uint32_t tile_bytes = kBTileBytes * nkb;
-    uint8_t* sRes = smem;                          // [2] resident tiles
-    uint8_t* sStg = smem + 2 * tile_bytes;         // [kBStages] streamed tiles
-    float* sDw = (float*)(sStg + kBStages * tile_bytes);  // [2][128] dw partials of half 1
-    uint64_t* bars = (uint64_t*)(sDw + 2 * 2 * kBT);
-    uint64_t* res_full = bars;                     // [2]
-    uint64_t* res_empty = bars + 2;                // [2]
-    uint64_t* k_full = bars + 4;                   // [kBStages]
+    const uint32_t stage_bytes = tile_bytes + (kGBytes + kWBytes + 1023u) / 1024u * 1024u;
+    uint8_t* sRes = smem;                          // [kBRes] resident tiles
+    uint8_t* sStg = smem + kBRes * tile_bytes;     // [kBStages] streamed tiles (+ G, w)
+    float* sDw = (float*)(sStg + kBStages * stage_bytes);  // [2][128] dw partials of column half 1
+    uint64_t* bars = (uint64_t*)(sDw + 2 * 4 * kBT);
+    uint64_t* res_full = bars;                     // [kBRes]
+    uint64_t* res_empty = bars + kBRes;            // [kBRes]
+    uint64_t* k_full = bars + 2 * kBRes;           // [kBStages]
     uint64_t* k_empty = k_full + kBStages;         // [kBStages]
     uint64_t* x_full = k_empty + kBStages;         // [kBRegions]
     uint64_t* p_full = x_full + kBRegions;         // [kBRegions]
     uint64_t* r_free = p_full + kBRegions;         // [kBRegions]
     uint64_t* acc_full = r_free + kBRegions;
     uint64_t* acc_empty = acc_full + 1;
-    uint64_t* dw_full = acc_empty + 1;             // [2] column half 1 -> half 0
-    uint64_t* dw_empty = dw_full + 2;              // [2] half 0 -> half 1
+    uint64_t* dw_full = acc_empty + 1;             // [2] column quarters 1..3 -> quarter 0
+    uint64_t* dw_empty = dw_full + 2;              // [2] quarter 0 -> quarters 1..3
     uint32_t* tmem_slot = (uint32_t*)(dw_empty + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kBRes; ++i) {
             mbar_init(res_full + i, 1);
             mbar_init(res_empty + i, 1);
         }
@@ -231,6 +248,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
         fence_mbar_init();
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
+        if constexpr (kStaged) tma_prefetch_desc(&tmg);
+        if constexpr (kStaged && MODE == 1) tma_prefetch_desc(&tmw);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -253,8 +272,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 if (u < 0) continue;
                 const BUnit un = bwd_unit<MODE>(p, u);
                 if (bwd_count<MODE>(p, un) == 0) continue;
-                const int ub = ucount & 1;
-                if (!(ok = mbar_wait(res_empty + ub, ((ucount >> 1) & 1) ^ 1, p.wait_ns))) break;
+                const int ub = ucount % kBRes;
+                if (!(ok = mbar_wait(res_empty + ub, ((ucount / kBRes) & 1) ^ 1, p.wait_ns))) break;
                 ++ucount;
                 mbar_arrive_expect_tx(res_full + ub, tile_bytes);
                 for (int kb = 0; kb < nkb; ++kb) {
@@ -269,14 +288,23 @@ __global__ void __launch_bounds__(kBThreads, 1)
                     const int st = kcount % kBStages;
                     if (!(ok = mbar_wait(k_empty + st, ((kcount / kBStages) & 1) ^ 1, p.wait_ns))) break;
                     ++kcount;
-                    mbar_arrive_expect_tx(k_full + st, tile_bytes);
+                    mbar_arrive_expect_tx(k_full + st, tile_bytes + kGBytes + kWBytes);
+                    uint8_t* sdst = sStg + st * stage_bytes;
                     for (int kb = 0; kb < nkb; ++kb) {
-                        uint8_t* dst = sStg + st * tile_bytes + kb * kBTileBytes;
+                        uint8_t* dst = sdst + kb * kBTileBytes;
                         if constexpr (MODE == 0)
                             tma_load_3d(dst, &tmk, k_full + st, kb * 64, un.b, x * kBT);
                         else
                             tma_load_4d(dst, &tmq, k_full + st, kb * 64, 0, un.b, x * QT);
                     }
+                    if constexpr (kStaged) {  // G [B,S,Skv_pad]: dims (Skv_pad, S, B)
+                        if constexpr (MODE == 0)
+                            tma_load_3d(sdst + tile_bytes, &tmg, k_full + st, x * kBT, un.res * QT, un.b);
+                        else
+                            tma_load_3d(sdst + tile_bytes, &tmg, k_full + st, un.res * kBT, x * QT, un.b);
+                    }
+                    if constexpr (kStaged && MODE == 1)  // w [S,B,H]: dims (H, B, S)
+                        tma_load_3d(sdst + tile_bytes + kGBytes, &tmw, k_full + st, 0, un.b, x * QT);
                 }
             }
         }
@@ -288,13 +316,13 @@ __global__ void __launch_bounds__(kBThreads, 1)
             const int nk = p.Dp / 16;
             // base descriptors of every buffer; a k-step adds its byte offset / 16 to the
             // 14-bit start-address field (shared addresses stay below 256 KB: no carry)
-            uint64_t rd[2], sd[kBStages], md[kBStages];
+            uint64_t rd[kBRes], sd[kBStages], md[kBStages];
 #pragma unroll
-            for (int j = 0; j < 2; ++j) rd[j] = smem_desc_kmajor(smem_u32(sRes + j * tile_bytes), 128);
+            for (int j = 0; j < kBRes; ++j) rd[j] = smem_desc_kmajor(smem_u32(sRes + j * tile_bytes), 128);
 #pragma unroll
             for (int j = 0; j < kBStages; ++j) {
-                sd[j] = smem_desc_kmajor(smem_u32(sStg + j * tile_bytes), 128);
-                md[j] = smem_desc_mn_sw128(smem_u32(sStg + j * tile_bytes), kBTileBytes);
+                sd[j] = smem_desc_kmajor(smem_u32(sStg + j * stage_bytes), 128);
+                md[j] = smem_desc_mn_sw128(smem_u32(sStg + j * stage_bytes), kBTileBytes);
             }
             auto koff16 = [](int k) {  // K-major k-step: 64-wide block, then 32 bytes per 16
                 return (uint64_t)((((k * 16) / 64) * kBTileBytes + ((k * 16) % 64) * 2) >> 4);
@@ -302,8 +330,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
             struct Pend {
                 int r, st, ub, tc, uc;
                 bool first, last;
-            } pend{};
-            bool have = false, ok = true;
+            };
+            bool ok = true;
             auto second = [&](const Pend& t) -> bool {
                 if (!mbar_wait(p_full + t.r, (t.tc / kBRegions) & 1, p.wait_ns)) return false;
                 if (t.first && !mbar_wait(acc_empty, (t.uc & 1) ^ 1, p.wait_ns)) return false;
@@ -327,6 +355,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 }
                 return true;
             };
+            Pend queue[kBLookahead];
+            int nq = 0;
             int kcount = 0, tcount = 0, ucount = 0;
             for (int i = 0; ok; ++i) {
                 const int u = bwd_unit_of(i, p.num_units);
@@ -335,8 +365,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 const BUnit un = bwd_unit<MODE>(p, u);
                 const int n = bwd_count<MODE>(p, un);
                 if (n == 0) continue;
-                const int ub = ucount & 1, uc = ucount;
-                if (!(ok = mbar_wait(res_full + ub, (ucount >> 1) & 1, p.wait_ns))) break;
+                const int ub = ucount % kBRes, uc = ucount;
+                if (!(ok = mbar_wait(res_full + ub, (ucount / kBRes) & 1, p.wait_ns))) break;
                 ++ucount;
                 int idx = 0;
                 for (int x = un.first; x < un.last; ++x) {
@@ -346,7 +376,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
                     if (!(ok = mbar_wait(r_free + r, ((tcount / kBRegions) & 1) ^ 1, p.wait_ns))) break;
                     tc_fence_after();
                     const uint32_t d = tmem_base + r * kBT;
-                    const uint64_t a0 = ub == 1 ? rd[1] : rd[0];
+                    const uint64_t a0 = ub == 2 ? rd[2] : (ub == 1 ? rd[1] : rd[0]);
                     uint64_t b0 = sd[0];
 #pragma unroll
                     for (int j = 1; j < kBStages; ++j) b0 = st == j ? sd[j] : b0;
@@ -354,20 +384,26 @@ __global__ void __launch_bounds__(kBThreads, 1)
                     for (int k = 0; k < 8; ++k)
                         if (k < nk) umma_f16(d, a0 + koff16(k), b0 + koff16(k), idesc_x, k > 0 ? 1u : 0u);
                     umma_commit(x_full + r);
-                    if (have && !(ok = second(pend))) break;
-                    pend = Pend{r, st, ub, tcount, uc, idx == 0, idx == n - 1};
-                    have = true;
+                    if (nq == kBLookahead) {
+                        if (!(ok = second(queue[0]))) break;
+#pragma unroll
+                        for (int j = 1; j < kBLookahead; ++j) queue[j - 1] = queue[j];
+                        --nq;
+                    }
+                    queue[nq++] = Pend{r, st, ub, tcount, uc, idx == 0, idx == n - 1};
                     ++kcount;
                     ++tcount;
                     ++idx;
                 }
             }
-            if (ok && have) second(pend);
+            for (int j = 0; ok && j < nq; ++j) ok = second(queue[j]);
         }
     } else {
         // --------------------------------------------------------- epilogue
+        // Two warps share each TMEM lane quadrant: warp half chalf takes columns
+        // [64*chalf, 64*chalf + 64) of X and of the accumulator.
         const int quad = warp & 3;           // TMEM lane quadrant this warp may read
-        const int half = (warp - 2) >> 2;    // columns [64*half, 64*half + 64)
+        const int chalf = (warp - 2) >> 2;
         const int row = quad * 32 + lane;    // TMEM lane = row of the resident tile
         const uint32_t lane_addr = tmem_base + ((uint32_t)(quad * 32) << 16);
         int tcount = 0, ucount = 0, done_units = 0;
@@ -390,92 +426,89 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 rvalid = true;  // partial rows past Skv are written and never read
             }
             const float wv = (MODE == 0 && rvalid) ? p.w[((size_t)s * p.B + un.b) * H + h] : 0.f;
-            float dw_acc = 0.f;
+            float dw4[4] = {0.f, 0.f, 0.f, 0.f};
             if (n > 0) {
                 for (int x = un.first; x < un.last; ++x) {
                     if (!bwd_active<MODE>(p, un, x)) continue;
                     const int r = tcount % kBRegions;
-                    if (!(ok = mbar_wait(x_full + r, (tcount / kBRegions) & 1, p.wait_ns))) break;
-                    ++tcount;
+                    const float* gS = (const float*)(sStg + (tcount % kBStages) * stage_bytes + tile_bytes);
+                    const float* wS = gS + QT * kBT;
+                    const int tc = tcount++;
+                    if (!(ok = mbar_wait(x_full + r, (tc / kBRegions) & 1, p.wait_ns))) break;
                     tc_fence_after();
 #pragma unroll 1
-                    for (int c = 2 * half; c < 2 * half + 2; ++c) {
-                        uint32_t xr[32];
-                        tmem_ld32(lane_addr + r * kBT + 32 * c, xr);
-                        float P[32];
-                        if constexpr (MODE == 0) {
-                            // columns = keys x*128 + 32c + i of this thread's query row
-                            float g[32];
-                            if (rvalid) {
-                                const float4* g4 = reinterpret_cast<const float4*>(
-                                    p.G + ((size_t)un.b * p.S + s) * p.Skv_pad + (size_t)x * kBT + 32 * c);
+                    for (int cc = 2 * chalf; cc < 2 * chalf + 2; ++cc) {
+                    const int c = cc;
+                    uint32_t xr[32];
+                    tmem_ld32(lane_addr + r * kBT + 32 * c, xr);
+                    float P[32];
+                    if constexpr (MODE == 0) {
+                        // columns = keys x*128 + 32c + i of this thread's query row
+                        float g[32];
+                        if (rvalid) {
+                            const float4* g4 = reinterpret_cast<const float4*>(
+                                kStaged ? gS + (row / H) * kBT + 32 * c
+                                        : p.G + ((size_t)un.b * p.S + s) * p.Skv_pad + (size_t)x * kBT +
+                                              32 * c);
 #pragma unroll
-                                for (int v = 0; v < 8; ++v) {
-                                    const float4 q4 = g4[v];
-                                    g[4 * v] = q4.x;
-                                    g[4 * v + 1] = q4.y;
-                                    g[4 * v + 2] = q4.z;
-                                    g[4 * v + 3] = q4.w;
-                                }
-                            } else {
-#pragma unroll
-                                for (int v = 0; v < 32; ++v) g[v] = 0.f;
-                            }
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int v = 0; v < 32; ++v) {
-                                const float xv = __uint_as_float(xr[v]);
-                                if (p.act == 0) {
-                                    dw_acc = fmaf(g[v], fmaxf(xv, 0.f), dw_acc);
-                                    P[v] = xv > 0.f ? g[v] * wv : 0.f;
-                                } else {
-                                    dw_acc = fmaf(g[v], xv, dw_acc);
-                                    P[v] = g[v] * wv;
-                                }
+                            for (int v = 0; v < 8; ++v) {
+                                const float4 q4 = g4[v];
+                                g[4 * v] = q4.x;
+                                g[4 * v + 1] = q4.y;
+                                g[4 * v + 2] = q4.z;
+                                g[4 * v + 3] = q4.w;
                             }
                         } else {
-                            // columns = (query, head) 32c + i of query tile x; this thread's key t
-                            float gw[32];
-                            if constexpr (H >= 32) {
-                                // one query per chunk: one grad, 32 consecutive weights
-                                const int sq = x * QT + (32 * c) / H;
-                                if (sq < p.S) {
-                                    const float g = p.G[((size_t)un.b * p.S + sq) * p.Skv_pad + t];
-                                    const float4* w4 = reinterpret_cast<const float4*>(
-                                        p.w + ((size_t)sq * p.B + un.b) * H + (32 * c) % H);
 #pragma unroll
-                                    for (int v = 0; v < 8; ++v) {
-                                        const float4 q4 = w4[v];
-                                        gw[4 * v] = g * q4.x;
-                                        gw[4 * v + 1] = g * q4.y;
-                                        gw[4 * v + 2] = g * q4.z;
-                                        gw[4 * v + 3] = g * q4.w;
-                                    }
-                                } else {
+                            for (int v = 0; v < 32; ++v) g[v] = 0.f;
+                        }
+                        tmem_ld_wait();
 #pragma unroll
-                                    for (int v = 0; v < 32; ++v) gw[v] = 0.f;
-                                }
+                        for (int v = 0; v < 32; ++v) {
+                            const float xv = __uint_as_float(xr[v]);
+                            if (p.act == 0) {
+                                dw4[v & 3] = fmaf(g[v], fmaxf(xv, 0.f), dw4[v & 3]);
+                                P[v] = xv > 0.f ? g[v] * wv : 0.f;
                             } else {
-#pragma unroll
-                                for (int v = 0; v < 32; ++v) {
-                                    const int col = 32 * c + v;
-                                    const int sq = x * QT + col / H, hq = col % H;
-                                    gw[v] = sq < p.S ? p.G[((size_t)un.b * p.S + sq) * p.Skv_pad + t] *
-                                                           p.w[((size_t)sq * p.B + un.b) * H + hq]
-                                                     : 0.f;
-                                }
-                            }
-                            tmem_ld_wait();
-#pragma unroll
-                            for (int v = 0; v < 32; ++v) {
-                                const float xv = __uint_as_float(xr[v]);
-                                P[v] = (p.act == 0) ? (xv > 0.f ? gw[v] : 0.f) : gw[v];
+                                dw4[v & 3] = fmaf(g[v], xv, dw4[v & 3]);
+                                P[v] = g[v] * wv;
                             }
                         }
-                        uint32_t hi[16], lo[16];
-                        split_hi_lo(P, hi, lo);
-                        tmem_st16(lane_addr + r * kBT + 32 * c, hi);
-                        tmem_st16(lane_addr + r * kBT + 32 * c + 16, lo);
+                    } else {
+                        // columns = (query, head) 32c + i of query tile x; this thread's key t
+                        float gw[32];
+                        if constexpr (kStaged) {
+                            // the stage holds this query tile's grads [QT][128] and weights
+                            // [QT][H] (zero past S): columns 32c .. 32c + 31
+#pragma unroll
+                            for (int v = 0; v < 32; v += 4) {
+                                const float4 w4 = *reinterpret_cast<const float4*>(wS + 32 * c + v);
+                                const float wv4[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e)
+                                    gw[v + e] = gS[((32 * c + v + e) / H) * kBT + row] * wv4[e];
+                            }
+                        } else {
+#pragma unroll
+                            for (int v = 0; v < 32; ++v) {
+                                const int col = 32 * c + v;
+                                const int sq = x * QT + col / H, hq = col % H;
+                                gw[v] = sq < p.S ? p.G[((size_t)un.b * p.S + sq) * p.Skv_pad + t] *
+                                                       p.w[((size_t)sq * p.B + un.b) * H + hq]
+                                                 : 0.f;
+                            }
+                        }
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int v = 0; v < 32; ++v) {
+                            const float xv = __uint_as_float(xr[v]);
+                            P[v] = (p.act == 0) ? (xv > 0.f ? gw[v] : 0.f) : gw[v];
+                        }
+                    }
+                    uint32_t hi[16], lo[16];
+                    split_hi_lo(P, hi, lo);
+                    tmem_st16(lane_addr + r * kBT + 32 * c, hi);
+                    tmem_st16(lane_addr + r * kBT + 32 * c + 16, lo);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -484,42 +517,35 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 }
                 if (!ok) break;
             }
-            // outputs of the unit: 64 columns of the accumulator per thread
-            float out[64];
+            // outputs of the unit: this warp's 64 columns of the accumulator, 32 at a time
             if (n > 0) {
                 if (!(ok = mbar_wait(acc_full, ucount & 1, p.wait_ns))) break;
                 ++ucount;
                 tc_fence_after();
+            }
+#pragma unroll 1
+            for (int c = 2 * chalf; c < 2 * chalf + 2; ++c) {
+            float out[32];
+            if (n > 0 && 32 * c < p.Dp) {
+                uint32_t ar[32];
+                tmem_ld32(lane_addr + acc_col + 32 * c, ar);
+                tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t ar[32];
-                    if (64 * half + 32 * c < p.Dp) {
-                        tmem_ld32(lane_addr + acc_col + 64 * half + 32 * c, ar);
-                        tmem_ld_wait();
-                    } else {
-#pragma unroll
-                        for (int v = 0; v < 32; ++v) ar[v] = 0u;
-                    }
-#pragma unroll
-                    for (int v = 0; v < 32; ++v) out[32 * c + v] = __uint_as_float(ar[v]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(acc_empty);
+                for (int v = 0; v < 32; ++v) out[v] = __uint_as_float(ar[v]);
             } else {
 #pragma unroll
-                for (int v = 0; v < 64; ++v) out[v] = 0.f;
+                for (int v = 0; v < 32; ++v) out[v] = 0.f;
             }
-            const int d0 = 64 * half;
-            const int dn = min(64, p.D - d0);  // valid output columns of this half
+            const int d0 = 32 * c;
+            const int dn = min(32, p.D - d0);  // valid output columns of this chunk
             if constexpr (MODE == 0) {
                 if (rvalid && dn > 0) {
                     const size_t o = (((size_t)s * p.B + un.b) * H + h) * p.D + d0;
                     if (p.grad_dtype == 0) {
                         float* dst = (float*)p.dq + o;
-                        if (dn == 64 && (p.D & 3) == 0) {
+                        if (dn == 32) {
 #pragma unroll
-                            for (int v = 0; v < 16; ++v)
+                            for (int v = 0; v < 8; ++v)
                                 reinterpret_cast<float4*>(dst)[v] =
                                     make_float4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
                         } else {
@@ -527,38 +553,53 @@ __global__ void __launch_bounds__(kBThreads, 1)
                         }
                     } else {
                         uint16_t* dst = (uint16_t*)p.dq + o;
-                        for (int v = 0; v < dn; v += 2) {
-                            const uint32_t pr = bf16x2_rn(out[v], v + 1 < dn ? out[v + 1] : 0.f);
-                            dst[v] = (uint16_t)(pr & 0xffffu);
-                            if (v + 1 < dn) dst[v + 1] = (uint16_t)(pr >> 16);
+                        if (dn == 32) {
+                            uint32_t pk[16];
+#pragma unroll
+                            for (int v = 0; v < 16; ++v) pk[v] = bf16x2_rn(out[2 * v], out[2 * v + 1]);
+#pragma unroll
+                            for (int v = 0; v < 4; ++v)
+                                reinterpret_cast<uint4*>(dst)[v] =
+                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                        } else {
+                            for (int v = 0; v < dn; ++v)
+                                dst[v] = (uint16_t)(bf16x2_rn(out[v], 0.f) & 0xffffu);
                         }
                     }
                 }
+            } else {
+                if (dn > 0 && d0 < p.Dp) {
+                    float* dst = p.part + ((size_t)u * kBT + row) * p.Dp + d0;
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        reinterpret_cast<float4*>(dst)[v] =
+                            make_float4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
+                }
+            }
+            }
+            if (n > 0) {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
+            }
+            if constexpr (MODE == 0) {
                 // dw: the two column halves' partial sums, added in a fixed order;
                 // half 1 hands its partial to half 0 through a double buffer
+                const float dw_acc = (dw4[0] + dw4[1]) + (dw4[2] + dw4[3]);
                 const int db = done_units & 1;
                 const uint32_t dph = (done_units >> 1) & 1;
                 float* dwb = sDw + db * kBT;
-                if (half == 1) {
+                if (chalf == 1) {
                     if (!(ok = mbar_wait(dw_empty + db, dph ^ 1, p.wait_ns))) break;
                     dwb[row] = dw_acc;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(dw_full + db);
                 } else {
                     if (!(ok = mbar_wait(dw_full + db, dph, p.wait_ns))) break;
-                    const float other = dwb[row];
+                    const float o1 = dwb[row];
                     __syncwarp();
                     if (lane == 0) mbar_arrive(dw_empty + db);
-                    if (rvalid) p.dw[((size_t)s * p.B + un.b) * H + h] = dw_acc + other;
-                }
-            } else {
-                if (dn > 0) {
-                    float* dst = p.part + ((size_t)u * kBT + row) * p.Dp + d0;
-#pragma unroll
-                    for (int v = 0; v < 16; ++v)
-                        if (4 * v < p.Dp - d0)
-                            reinterpret_cast<float4*>(dst)[v] =
-                                make_float4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
+                    if (rvalid) p.dw[((size_t)s * p.B + un.b) * H + h] = dw_acc + o1;
                 }
             }
             ++done_units;
@@ -616,15 +657,23 @@ __global__ void __launch_bounds__(kScatterThreads)
     }
 }
 
-// First partial-dk unit of each key tile within a batch (table size ntk + 1).
-struct UnitTable {
-    int pre[kBMaxKeyTiles + 1];
+// First partial-dk unit of each chunk of query tiles within a batch.
+struct ChunkTable {
+    int cpre[kBMaxChunks + 1];
 };
 
-// dk[t,b,:] = sum over the key tile's chunks c of part[unit(b, t/128, c)][t%128][:],
+// Chunk of the first query tile that sees key tile kt, or nchunks when none does.
+__host__ __device__ __forceinline__ int bwd_c0(bool causal, int kt, int ratio, int QT, int qtiles,
+                                               int CH, int nchunks) {
+    const int qlo = bwd_qlo(causal, kt, ratio, QT);
+    return qlo < qtiles ? qlo / CH : nchunks;
+}
+
+// dk[t,b,:] = sum over the chunks c of key tile t/128 of part[unit(b, c, t/128)][t%128][:],
 // in chunk order.
 __global__ void bwd_reduce_kernel(const float* __restrict__ part, int B, int Skv, int D, int Dp, int U,
-                                  const __grid_constant__ UnitTable tab, int grad_dtype, void* dk) {
+                                  const __grid_constant__ ChunkTable tab, int nchunks, int CH, int QT,
+                                  int qtiles, int ratio, int causal, int grad_dtype, void* dk) {
     const int D4 = D / 4;
     const int64_t n = (int64_t)B * Skv * D4;
     for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
@@ -633,9 +682,9 @@ __global__ void bwd_reduce_kernel(const float* __restrict__ part, int B, int Skv
         const int64_t bt = e / D4;
         const int t = (int)(bt % Skv), b = (int)(bt / Skv);
         const int kt = t / kBT, tl = t % kBT;
-        const int u0 = b * U + tab.pre[kt], u1 = b * U + tab.pre[kt + 1];
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int u = u0; u < u1; ++u) {
+        for (int c = bwd_c0(causal != 0, kt, ratio, QT, qtiles, CH, nchunks); c < nchunks; ++c) {
+            const int u = b * U + tab.cpre[c] + kt;
             const float4 v = *reinterpret_cast<const float4*>(part + ((size_t)u * kBT + tl) * Dp + d4);
             acc.x += v.x;
             acc.y += v.y;
@@ -656,12 +705,14 @@ __global__ void bwd_reduce_kernel(const float* __restrict__ part, int B, int Skv
 LIDX_STATUS_READER(status_bwd)
 
 struct BwdPlan {
-    int Dp, QT, qtiles, ntk, Skv_pad, CH, U, nkb;
+    int Dp, QT, qtiles, ntk, Skv_pad, CH, U, nkb, nchunks;
     size_t g_bytes, part_bytes;
-    int pre[kBMaxKeyTiles + 1];
+    int cpre[kBMaxChunks + 1];
 };
 
-// Tiling of the backward; `causal` selects the first query tile of each key tile.
+// Tiling of the backward.  Key-major units: chunk c of query tiles [c*CH, (c+1)*CH)
+// holds one unit per key tile that some row of the chunk sees; `causal` gives each
+// key tile its first visible query tile (explicit ranges: every tile).
 static void bwd_plan(int64_t B, int64_t S, int64_t Skv, int H, int D, int ratio, bool causal, int sms,
                      BwdPlan& pl) {
     pl.Dp = (D + 63) / 64 * 64;
@@ -670,40 +721,40 @@ static void bwd_plan(int64_t B, int64_t S, int64_t Skv, int H, int D, int ratio,
     pl.qtiles = (int)((S + pl.QT - 1) / pl.QT);
     pl.ntk = (int)((Skv + kBT - 1) / kBT);
     pl.Skv_pad = pl.ntk * kBT;
-    // query tiles per key tile, then chunks of CH so that there are about 4 units per SM
-    int64_t T = 0;
+    int64_t T = 0;  // (query tile, key tile) pairs
     for (int kt = 0; kt < pl.ntk; ++kt) {
-        int qlo = 0;
-        if (causal) qlo = (int)((((int64_t)kt * kBT + 1) * ratio - 1) / pl.QT);
+        const int qlo = bwd_qlo(causal, kt, ratio, pl.QT);
         T += qlo < pl.qtiles ? pl.qtiles - qlo : 0;
     }
     T *= B;
-    const int64_t target = 4 * (int64_t)sms;
+    const int64_t target = 4 * (int64_t)sms;  // about four units per SM
     pl.CH = (int)((T + target - 1) / target);
+    const int ch_min = (pl.qtiles + kBMaxChunks - 1) / kBMaxChunks;
+    if (pl.CH < ch_min) pl.CH = ch_min;
     if (pl.CH < 1) pl.CH = 1;
-    int U = 0;
-    for (int kt = 0; kt < pl.ntk; ++kt) {
-        pl.pre[kt] = U;
-        int qlo = 0;
-        if (causal) qlo = (int)((((int64_t)kt * kBT + 1) * ratio - 1) / pl.QT);
-        const int nq = qlo < pl.qtiles ? pl.qtiles - qlo : 0;
-        U += (nq + pl.CH - 1) / pl.CH;
+    pl.nchunks = (pl.qtiles + pl.CH - 1) / pl.CH;
+    int U = 0, kt = 0;
+    for (int c = 0; c < pl.nchunks; ++c) {
+        while (kt < pl.ntk && bwd_c0(causal, kt, ratio, pl.QT, pl.qtiles, pl.CH, pl.nchunks) <= c) ++kt;
+        pl.cpre[c] = U;
+        U += kt;  // key tiles 0 .. kt-1 have a unit in chunk c
     }
-    pl.pre[pl.ntk] = U;
+    pl.cpre[pl.nchunks] = U;
     pl.U = U;
     pl.g_bytes = ((size_t)B * S * pl.Skv_pad * 4 + 255) / 256 * 256;
     pl.part_bytes = (size_t)B * U * kBT * pl.Dp * 4;
 }
 
-// Partial dk units per batch are at most T/CH + ntk <= 4*sms/B + ntk, whatever
-// the ranges, so this bound holds for causal and explicit-range calls alike.
+// Units per batch are sum over key tiles of (chunks from its first one on) <=
+// T/(B*CH) + 2*ntk, and T/CH <= 4*sms: the bound holds for causal and
+// explicit-range calls alike.
 size_t bwd_workspace_bytes(int64_t B, int64_t S, int64_t Skv, int H, int D, int topk, int num_sms) {
     (void)topk;
     if (B <= 0 || S <= 0 || Skv <= 0 || H < 1 || H > 128) return 0;
     const int64_t Dp = (D + 63) / 64 * 64;
     const int64_t ntk = (Skv + kBT - 1) / kBT;
     const size_t g = ((size_t)B * S * ntk * kBT * 4 + 255) / 256 * 256;
-    const size_t units = (size_t)4 * num_sms + (size_t)B * ntk;
+    const size_t units = (size_t)4 * num_sms + (size_t)2 * B * ntk;
     return g + units * kBT * Dp * 4;
 }
 
@@ -727,36 +778,60 @@ static int encode_bwd_maps(const BwdLaunch& a, CUtensorMap* mq, CUtensorMap* mk,
     return 0;
 }
 
-static size_t bwd_smem_bytes(int nkb) {
-    return 1024 + (size_t)(2 + kBStages) * kBTileBytes * nkb + 2 * 2 * kBT * 4 + 32 * 8 + 16;
+// G [B,S,Skv_pad] fp32 as dims (Skv_pad, S, B), box [QT rows][128 keys]; w [S,B,H]
+// fp32 as dims (H, B, S), box [QT queries][H].  Used when H >= 8.
+static int encode_stage_maps(const BwdLaunch& a, const float* G, int Skv_pad, int QT, CUtensorMap* mg,
+                             CUtensorMap* mw) {
+    cuuint32_t es[3] = {1, 1, 1};
+    cuuint64_t gdim[3] = {(cuuint64_t)Skv_pad, (cuuint64_t)a.S, (cuuint64_t)a.B};
+    cuuint64_t gstr[2] = {(cuuint64_t)Skv_pad * 4, (cuuint64_t)a.S * Skv_pad * 4};
+    cuuint32_t gbox[3] = {(cuuint32_t)kBT, (cuuint32_t)QT, 1};
+    if (encode_tiled(mg, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, (void*)G, gdim, gstr, gbox, es,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return 1;
+    cuuint64_t wdim[3] = {(cuuint64_t)a.H, (cuuint64_t)a.B, (cuuint64_t)a.S};
+    cuuint64_t wstr[2] = {(cuuint64_t)a.H * 4, (cuuint64_t)a.B * a.H * 4};
+    cuuint32_t wbox[3] = {(cuuint32_t)a.H, 1, (cuuint32_t)QT};
+    if (encode_tiled(mw, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, (void*)a.w, wdim, wstr, wbox, es,
+                     CU_TENSOR_MAP_SWIZZLE_NONE))
+        return 1;
+    return 0;
+}
+
+static size_t bwd_smem_bytes(int nkb, int H, int MODE) {
+    const size_t tile = (size_t)kBTileBytes * nkb;
+    size_t extra = 0;
+    if (H >= 8) extra = ((size_t)(kBT / H) * kBT * 4 + (MODE == 1 ? (size_t)kBT * 4 : 0) + 1023) / 1024 * 1024;
+    return 1024 + kBRes * tile + kBStages * (tile + extra) + 2 * 4 * kBT * 4 + 32 * 8 + 16;
 }
 
 template <int H>
-static cudaError_t bwd_tiles_h(const CUtensorMap& mq, const CUtensorMap& mk, const BwdParams& p0,
-                               const BwdLaunch& a) {
-    // at least 120 KB so that one CTA (and its 512 TMEM columns) owns each SM
-    int smem = (int)bwd_smem_bytes(p0.nkb);
-    if (smem < 120 * 1024) smem = 120 * 1024;
+static cudaError_t bwd_tiles_h(const CUtensorMap* maps, const BwdParams& p0, const BwdLaunch& a) {
     BwdParams p = p0;
-    // dq and dw, query-major
+    // dq and dw, query-major; at least 120 KB of shared memory so that one CTA
+    // (and its 512 TMEM columns) owns each SM
     {
+        int smem = (int)bwd_smem_bytes(p.nkb, H, 0);
+        if (smem < 120 * 1024) smem = 120 * 1024;
         auto kern = bwd_tile_kernel<H, 0>;
         cudaError_t e = set_smem_attr((const void*)kern, smem);
         if (e != cudaSuccess) return e;
         p.num_units = p.B * p.qtiles;
         const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
-        if (grid > 0) kern<<<grid, kBThreads, smem, a.stream>>>(mq, mk, p);
+        if (grid > 0) kern<<<grid, kBThreads, smem, a.stream>>>(maps[0], maps[1], maps[2], maps[3], p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
     // partial dk, key-major
     {
+        int smem = (int)bwd_smem_bytes(p.nkb, H, 1);
+        if (smem < 120 * 1024) smem = 120 * 1024;
         auto kern = bwd_tile_kernel<H, 1>;
         cudaError_t e = set_smem_attr((const void*)kern, smem);
         if (e != cudaSuccess) return e;
         p.num_units = p.B * p.U;
         const int grid = p.num_units < a.num_sms ? p.num_units : a.num_sms;
-        if (grid > 0) kern<<<grid, kBThreads, smem, a.stream>>>(mq, mk, p);
+        if (grid > 0) kern<<<grid, kBThreads, smem, a.stream>>>(maps[0], maps[1], maps[2], maps[3], p);
         return cudaGetLastError();
     }
 }
@@ -793,8 +868,14 @@ cudaError_t bwd_launch(const BwdLaunch& a) {
         if (e != cudaSuccess) return e;
     }
     // 2, 3. tensor-core tiles
-    CUtensorMap mq, mk;
-    if (encode_bwd_maps(a, &mq, &mk, pl.QT)) return cudaErrorInvalidValue;
+    CUtensorMap maps[4];
+    if (encode_bwd_maps(a, &maps[0], &maps[1], pl.QT)) return cudaErrorInvalidValue;
+    if (a.H >= 8) {
+        if (encode_stage_maps(a, G, pl.Skv_pad, pl.QT, &maps[2], &maps[3])) return cudaErrorInvalidValue;
+    } else {
+        maps[2] = maps[0];  // not read
+        maps[3] = maps[0];
+    }
     BwdParams p;
     memset(&p, 0, sizeof p);
     p.B = a.B;
@@ -820,29 +901,31 @@ cudaError_t bwd_launch(const BwdLaunch& a) {
     p.QT = pl.QT;
     p.U = pl.U;
     p.CH = pl.CH;
+    p.nchunks = pl.nchunks;
     p.wait_ns = wait_limit_ns();
-    memcpy(p.pre, pl.pre, sizeof(int) * (pl.ntk + 1));
+    memcpy(p.cpre, pl.cpre, sizeof(int) * (pl.nchunks + 1));
     cudaError_t e;
     switch (a.H) {
-        case 1: e = bwd_tiles_h<1>(mq, mk, p, a); break;
-        case 2: e = bwd_tiles_h<2>(mq, mk, p, a); break;
-        case 4: e = bwd_tiles_h<4>(mq, mk, p, a); break;
-        case 8: e = bwd_tiles_h<8>(mq, mk, p, a); break;
-        case 16: e = bwd_tiles_h<16>(mq, mk, p, a); break;
-        case 32: e = bwd_tiles_h<32>(mq, mk, p, a); break;
-        case 64: e = bwd_tiles_h<64>(mq, mk, p, a); break;
-        case 128: e = bwd_tiles_h<128>(mq, mk, p, a); break;
+        case 1: e = bwd_tiles_h<1>(maps, p, a); break;
+        case 2: e = bwd_tiles_h<2>(maps, p, a); break;
+        case 4: e = bwd_tiles_h<4>(maps, p, a); break;
+        case 8: e = bwd_tiles_h<8>(maps, p, a); break;
+        case 16: e = bwd_tiles_h<16>(maps, p, a); break;
+        case 32: e = bwd_tiles_h<32>(maps, p, a); break;
+        case 64: e = bwd_tiles_h<64>(maps, p, a); break;
+        case 128: e = bwd_tiles_h<128>(maps, p, a); break;
         default: e = cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
     // 4. fixed-order reduction of the partial dk
-    UnitTable tab;
-    memcpy(tab.pre, pl.pre, sizeof(int) * (pl.ntk + 1));
+    ChunkTable tab;
+    memcpy(tab.cpre, pl.cpre, sizeof(int) * (pl.nchunks + 1));
     const int64_t n = (int64_t)a.B * a.Skv * (a.D / 4);
     int64_t grid = (n + 255) / 256;
     if (grid > (int64_t)a.num_sms * 8) grid = (int64_t)a.num_sms * 8;
     bwd_reduce_kernel<<<(unsigned)grid, 256, 0, a.stream>>>(part, a.B, a.Skv, a.D, pl.Dp, pl.U, tab,
-                                                           a.grad_dtype, a.dk);
+                                                           pl.nchunks, pl.CH, pl.QT, pl.qtiles, a.ratio,
+                                                           a.ks == nullptr ? 1 : 0, a.grad_dtype, a.dk);
     return cudaGetLastError();
 }
 

@@ -253,8 +253,9 @@ def test_context_parallel_shards_on_the_cuda_path(ranks):
     """Host-simulated context-parallel ranks: each holds a contiguous shard of
     query rows (global positions p0..p0+S_r) and every compressed key, and calls
     the library with its own causal ranges.  The shards' forward outputs
-    concatenate to the unsharded call bit for bit; their dq and dw equal the
-    unsharded ones, and their partial dk sum to the full dk."""
+    concatenate to the unsharded call bit for bit; their dq equals the
+    unsharded one bit for bit and their dw up to fp32 reassociation, and their
+    partial dk sum to the full dk."""
     wl = workloads.WORKLOADS["c4_fwd"].with_(S=2048, Skv=512, topk=256)
     q, k, w = workloads.v4_inputs(wl, 4)
     qd, kd, wd = cuda(q, k, w)
@@ -274,7 +275,10 @@ def test_context_parallel_shards_on_the_cuda_path(ranks):
         assert torch.equal(i_r, full_i[:, p0:p1]) and torch.equal(s_r, full_s[:, p0:p1])
         dq_r, dk_r, dw_r = lidx.lidx_indexer_bwd_ranges(qs, kd, ws_, i_r, grad[:, p0:p1].contiguous(),
                                                         ks, ke)
-        assert torch.equal(dq_r, fdq[p0:p1]) and torch.equal(dw_r, fdw[p0:p1])
+        assert torch.equal(dq_r, fdq[p0:p1])
+        # dw sums a row's key tiles in an order that follows the CTA's schedule:
+        # equal up to fp32 reassociation
+        assert torch.allclose(dw_r, fdw[p0:p1], rtol=1e-5, atol=1e-6 * fdw.abs().max().item())
         dk_sum += dk_r
     torch.cuda.synchronize()
     assert lidx.lidx_device_status() == 0
