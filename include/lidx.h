@@ -184,7 +184,7 @@ int lidx_topk_rows(const float* logits, int64_t rows, int64_t S, int64_t Skv,
  *   scores_out bf16 [B,S,Skv]: where allowed[b,s,t] != 0,
  *       bf16( sum_h  bf16( act(bf16(q.k)) * w ) )   (fp32 head reduction),
  *   and -inf (0xFF80) elsewhere.  allowed needs no alignment.
- *   workspace: lidx_workspace_bytes(LIDX_OP_SCORES_V41, ...) bytes.
+ *   workspace: lidx_workspace_bytes(LIDX_OP_SCORES_V41, ...) bytes, 256-byte aligned.
  */
 int lidx_indexer_scores_v41(const void* q, const void* k, const void* w,
                             const uint8_t* allowed, int64_t B, int64_t S, int64_t Skv,

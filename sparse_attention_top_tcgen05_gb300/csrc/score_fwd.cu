@@ -26,6 +26,7 @@
 //     tile's queries are prefetched into L2 while the current one is swept.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <string.h>
 #include <stdint.h>
 
 #include "kernels.h"
@@ -46,11 +47,13 @@ constexpr int kEpiBar = 1;         // named barrier id of the epilogue group
 constexpr int kTopkBar = 2;        // named barrier ids of the selection groups: 2, 3, 4
 constexpr int kTopkGroups = 3;     // rows selected concurrently
 constexpr int kTopkGroupThreads = kTopkThreads / kTopkGroups;
+constexpr int kVisStages = 4;      // V4.1: ring of staged visibility blocks
 
 struct Unit {
     int b, s0, qt;
     int lo_t, hi_t;  // key tiles [lo_t, hi_t) with work
     int lo_k, hi_k;  // visible keys of the tile's union range
+    uint64_t bits;   // V4.1: bit j set when key tile lo_t + j has a visible pair
 };
 
 __device__ __forceinline__ void row_range(const ScoreParams& p, int s, int& lo, int& hi) {
@@ -66,24 +69,19 @@ __device__ __forceinline__ void row_range(const ScoreParams& p, int s, int& lo, 
 }
 
 template <int QT, bool V41>
-__device__ __forceinline__ Unit make_unit(const ScoreParams& p, int u) {
+__device__ __forceinline__ Unit make_unit(const ScoreParams& p, int u, const int4& rec) {
     Unit un;
+    un.bits = 0;
     const int qt = p.qtiles - 1 - u / p.B;  // heaviest (latest) query tiles first
     un.b = u % p.B;
     un.qt = qt;
     un.s0 = qt * QT;
     const int s_last = min(un.s0 + QT - 1, p.S - 1);
     if constexpr (V41) {
-        // key tiles with any visible pair come from the visibility tile map
-        const uint8_t* m = p.tilemap + ((size_t)un.b * p.qtiles + qt) * p.ntk;
-        int first = -1, last = -1;
-        for (int kt = 0; kt < p.ntk; ++kt)
-            if (m[kt]) {
-                if (first < 0) first = kt;
-                last = kt;
-            }
-        un.lo_t = first < 0 ? 0 : first;
-        un.hi_t = first < 0 ? 0 : last + 1;
+        // the range of key tiles with visible pairs comes from the visibility pass
+        un.lo_t = rec.x;
+        un.hi_t = rec.y;
+        un.bits = (uint64_t)(uint32_t)rec.z | ((uint64_t)(uint32_t)rec.w << 32);
         un.lo_k = un.lo_t * kM;
         un.hi_k = min(un.hi_t * kM, p.Skv);
         return un;
@@ -117,7 +115,11 @@ __device__ __forceinline__ Unit make_unit(const ScoreParams& p, int u) {
 
 template <bool V41>
 __device__ __forceinline__ bool tile_active(const ScoreParams& p, const Unit& un, int kt) {
-    if constexpr (V41) return p.tilemap[((size_t)un.b * p.qtiles + un.qt) * p.ntk + kt] != 0;
+    if constexpr (V41) {
+        const int j = kt - un.lo_t;
+        if (j < 64) return (un.bits >> j) & 1u;
+        return p.tilemap[((size_t)un.b * p.qtiles + un.qt) * p.ntk + kt] != 0;
+    }
     return true;
 }
 
@@ -128,6 +130,32 @@ __device__ __forceinline__ int unit_of(int i, int num_units) {
     if (base >= num_units) return -2;
     const int u = base + ((i & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
     return u < num_units ? u : -1;
+}
+
+// V4.1: the visibility record of this CTA's i-th unit (zeros where there is
+// none).  Each role loads the next unit's record one step ahead, so that the
+// load's latency overlaps the current unit.
+template <bool V41>
+__device__ __forceinline__ int4 unit_rec(const ScoreParams& p, int i) {
+    if constexpr (V41) {
+        const int u = unit_of(i, p.num_units);
+        if (u >= 0) return p.urec[(size_t)(u % p.B) * p.qtiles + (p.qtiles - 1 - u / p.B)];
+    }
+    return make_int4(0, 0, 0, 0);
+}
+
+// V4.1: word e of a unit's bf16 weights, laid out as the epilogue keeps them:
+// heads (2e, 2e+1) of query 2e / H in one word (one weight per word at H = 1);
+// zero past the sequence, for threads past the tile's words and for u < 0.
+template <int H, int QT>
+__device__ __forceinline__ uint32_t v41_weight_word(const ScoreParams& p, int u, int e) {
+    constexpr int WPER = H >= 2 ? 2 : 1;
+    if (u < 0 || e >= kN / WPER) return 0u;
+    const int b = u % p.B, s = (p.qtiles - 1 - u / p.B) * QT + (WPER * e) / H, h = (WPER * e) % H;
+    if (s >= p.S) return 0u;
+    const uint16_t* wr = p.w16 + ((size_t)b * p.S + s) * H + h;
+    if constexpr (WPER == 2) return *reinterpret_cast<const uint32_t*>(wr);  // h even: 4-byte aligned
+    return (uint32_t)wr[0];
 }
 
 __device__ __forceinline__ float act_f(float x, int act) { return act == 0 ? fmaxf(x, 0.f) : x; }
@@ -210,20 +238,30 @@ __device__ __forceinline__ float head_sum(const uint32_t (&r)[NR], const float* 
     }
 }
 
+// (bf16(hi) << 16) | bf16(lo), round to nearest even; RELU: negative results
+// become +0 (the same as ReLU of the rounded values, up to the sign of zero,
+// which a sum that starts from +0 does not see)
+template <bool RELU>
 __device__ __forceinline__ uint32_t cvt_bf16x2(float hi, float lo) {
     uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-__device__ __forceinline__ uint32_t max_bf16x2(uint32_t a, uint32_t b) {
-    uint32_t r;
-    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    if constexpr (RELU)
+        asm("cvt.rn.relu.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    else
+        asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
 __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
+}
+// s0 += float(low half of z2), s1 += float(high half), each one fp32 add
+// (the widening of a bf16 value to fp32 is exact)
+__device__ __forceinline__ void add_bf16x2_f32(uint32_t z2, float& s0, float& s1) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "r"(z2));
 }
 __device__ __forceinline__ float bf16_round_f(float x) {
     uint32_t r;
@@ -236,23 +274,34 @@ __device__ __forceinline__ float bf16_round_f(float x) {
 // wp holds the query's bf16 weights as pairs (low half = even head); for H = 1
 // one weight per word.  The product of two bf16 values is exact, so rounding it
 // once to bf16 is the stated rounding of the weighted head score.
-template <int H, int NR>
-__device__ __forceinline__ float head_sum_v41(const uint32_t (&r)[NR], int c0, const uint32_t* wp,
-                                              int act) {
+template <int H, bool RELU, int NR>
+__device__ __forceinline__ float head_sum_v41(const uint32_t (&r)[NR], int c0, const uint32_t* wp) {
     if constexpr (H >= 2) {
+        constexpr int WV = H >= 8 ? 4 : H / 2;  // weight words per shared-memory load
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int h = 0; h < H; h += 2) {
-            uint32_t y2 = cvt_bf16x2(__uint_as_float(r[c0 + h + 1]), __uint_as_float(r[c0 + h]));
-            if (act == 0) y2 = max_bf16x2(y2, 0u);
-            const uint32_t z2 = mul_bf16x2(y2, wp[h / 2]);
-            s0 += __uint_as_float(z2 << 16);
-            s1 += __uint_as_float(z2 & 0xffff0000u);
+        for (int h = 0; h < H; h += 2 * WV) {
+            uint32_t wv[WV];
+            if constexpr (WV == 4) {
+                const uint4 t = *reinterpret_cast<const uint4*>(wp + h / 2);
+                wv[0] = t.x, wv[1] = t.y, wv[2] = t.z, wv[3] = t.w;
+            } else if constexpr (WV == 2) {
+                const uint2 t = *reinterpret_cast<const uint2*>(wp + h / 2);
+                wv[0] = t.x, wv[1] = t.y;
+            } else {
+                wv[0] = wp[h / 2];
+            }
+#pragma unroll
+            for (int j = 0; j < WV; ++j) {
+                const int c = c0 + h + 2 * j;
+                const uint32_t y2 = cvt_bf16x2<RELU>(__uint_as_float(r[c + 1]), __uint_as_float(r[c]));
+                add_bf16x2_f32(mul_bf16x2(y2, wv[j]), s0, s1);
+            }
         }
         return s0 + s1;
     } else {
         float y = bf16_round_f(__uint_as_float(r[c0]));
-        if (act == 0) y = fmaxf(y, 0.f);
+        if (RELU) y = fmaxf(y, 0.f);
         return bf16_round_f(y * __uint_as_float(wp[0] << 16));
     }
 }
@@ -277,7 +326,7 @@ __device__ __forceinline__ void row_gather(const float* row, int lo, int hi, con
 template <int H, bool V41>
 __global__ void __launch_bounds__(kThreads, 1)
     score_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
-                     const ScoreParams p) {
+                     const __grid_constant__ CUtensorMap tma, const ScoreParams p) {
     constexpr int QT = kN / H;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, formed by pointer arithmetic on the shared array
@@ -290,8 +339,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     int* sLo = (int*)(smem + L.range_off);
     int* sHi = sLo + kN;
     uint64_t* bars = (uint64_t*)(smem + L.bar_off);
-    uint64_t* q_full = bars + 0;
-    uint64_t* q_empty = bars + 1;
+    // V4.1 keeps two query tiles: the second lives in the selection scratch, which
+    // V4.1 does not use, so that the next unit's queries load during this unit's
+    // key sweep.  V4 keeps one.
+    constexpr int NQB = V41 ? 2 : 1;
+    static_assert(2 + 2 * kStages + 8 <= 14, "second query barriers overlap the ring barriers");
+    // V4.1 spreads the epilogue over 16 warps of 64 accumulator columns when a
+    // query's heads fit in 64 columns (the selection warps have no work there)
+    constexpr int EW = (V41 && H <= 64) ? 16 : kEpiWarps;
+    constexpr int EWT = 32 * EW;
+    static_assert(2 + EW <= kThreads / 32, "epilogue warps exceed the block");
+    // V4.1 (QT <= 32): the visibility flags of each computed block, QT rows of
+    // 128 bytes, come by TMA into a ring after the second query tile
+    constexpr bool VIS_RING = V41 && QT <= 32;
+    // then each epilogue warp's own copy of its weights (up to 64 words a warp)
+    static_assert(kTopkGroups * ((sizeof(TopkSmem) + 15) / 16 * 16) >=
+                      (size_t)kN * 128 * 2 + kVisStages * 32 * kM + 16 * 64 * 4,
+                  "second query tile, visibility ring and weights exceed the scratch");
+    const bool vis_tma = VIS_RING && p.vis_tma;
+    uint8_t* const sQ1 = smem + L.topk_off;  // second query tile (V4.1 only)
+    uint8_t* const sVis = sQ1 + kN * p.D * 2;
+    uint32_t* const sWw = reinterpret_cast<uint32_t*>(sVis + kVisStages * 32 * kM);  // [EW][64]
+    uint64_t* vis_full = bars + 16;   // [kVisStages]
+    uint64_t* vis_empty = bars + 20;  // [kVisStages]
+    auto sQb = [&](int qb) { return qb ? sQ1 : sQ; };
+    auto q_fullv = [&](int qb) { return bars + (qb ? 14 : 0); };
+    auto q_emptyv = [&](int qb) { return bars + (qb ? 15 : 1); };
     uint64_t* k_full = bars + 2;                  // [kStages]
     uint64_t* k_empty = bars + 2 + kStages;       // [kStages]
     uint64_t* acc_full = bars + 2 + 2 * kStages;  // [2]
@@ -306,21 +379,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool select = !V41 && p.topk > 0;
 
     if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(q_empty, 1);
+        for (int i = 0; i < NQB; ++i) {
+            mbar_init(q_fullv(i), 1);
+            mbar_init(q_emptyv(i), 1);
+        }
         for (int i = 0; i < kStages; ++i) {
             mbar_init(k_full + i, 1);
             mbar_init(k_empty + i, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(acc_full + i, 1);
-            mbar_init(acc_empty + i, kEpiWarps);
+            mbar_init(acc_empty + i, EW);
             mbar_init(rows_full + i, kEpiThreads);
             mbar_init(rows_empty + i, QT);  // one arrival per selected row
         }
+        if (vis_tma)
+            for (int i = 0; i < kVisStages; ++i) {
+                mbar_init(vis_full + i, 1);
+                mbar_init(vis_empty + i, EW);
+            }
         fence_mbar_init();
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
+        if (vis_tma) tma_prefetch_desc(&tma);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, 512);
@@ -336,21 +417,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0 && !p.debug_stall) {
             int kcount = 0, qcount = 0;
             bool ok = true;
+            int4 rec_next = unit_rec<V41>(p, 0);
             for (int i = 0; ok; ++i) {
                 const int u = unit_of(i, p.num_units);
                 if (u == -2) break;
+                const int4 rec = rec_next;
+                rec_next = unit_rec<V41>(p, i + 1);
                 if (u < 0) continue;
-                const Unit un = make_unit<QT, V41>(p, u);
+                const Unit un = make_unit<QT, V41>(p, u, rec);
                 if (un.hi_t <= un.lo_t) continue;
-                if (!(ok = mbar_wait(q_empty, (qcount & 1) ^ 1, p.wait_ns))) break;
+                const int qb = qcount % NQB;
+                if (!(ok = mbar_wait(q_emptyv(qb), ((qcount / NQB) & 1) ^ 1, p.wait_ns))) break;
                 ++qcount;
-                mbar_arrive_expect_tx(q_full, kN * p.D * 2);
+                mbar_arrive_expect_tx(q_fullv(qb), kN * p.D * 2);
                 for (int kb = 0; kb < nkb; ++kb)
                 {
                     if constexpr (V41)  // q [B,S,H,D]: dims (D, H, S, B)
-                        tma_load_4d(sQ + kb * kN * swz, &tmq, q_full, kb * KB, 0, un.s0, un.b);
+                        tma_load_4d(sQb(qb) + kb * kN * swz, &tmq, q_fullv(qb), kb * KB, 0, un.s0, un.b);
                     else  // q [S,B,H,D]: dims (D, H, B, S)
-                        tma_load_4d(sQ + kb * kN * swz, &tmq, q_full, kb * KB, 0, un.b, un.s0);
+                        tma_load_4d(sQb(qb) + kb * kN * swz, &tmq, q_fullv(qb), kb * KB, 0, un.b, un.s0);
                 }
                 // warm L2 with the next query tile of this CTA
                 const int un2 = unit_of(i + 1, p.num_units);
@@ -366,9 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int kt = un.lo_t; kt < un.hi_t; ++kt) {
                     if (!tile_active<V41>(p, un, kt)) continue;
-                    const int st = kcount % kStages;
-                    if (!(ok = mbar_wait(k_empty + st, ((kcount / kStages) & 1) ^ 1, p.wait_ns))) break;
-                    ++kcount;
+                    const int kc = kcount++, st = kc % kStages;
+                    if (!(ok = mbar_wait(k_empty + st, ((kc / kStages) & 1) ^ 1, p.wait_ns))) break;
                     uint8_t* dst = sK + st * kM * p.D * 2;
                     mbar_arrive_expect_tx(k_full + st, kM * p.D * 2);
                     for (int kb = 0; kb < nkb; ++kb) {
@@ -376,6 +460,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_3d(dst + kb * kM * swz, &tmk, k_full + st, kb * KB, kt * kM, un.b);
                         else  // k [Skv,B,D]: dims (D, B, Skv)
                             tma_load_3d(dst + kb * kM * swz, &tmk, k_full + st, kb * KB, un.b, kt * kM);
+                    }
+                    if (vis_tma) {  // allowed [B,S,Skv]: dims (Skv, S, B); zero past the ends
+                        const int vs = kc % kVisStages;
+                        if (!(ok = mbar_wait(vis_empty + vs, ((kc / kVisStages) & 1) ^ 1, p.wait_ns))) break;
+                        mbar_arrive_expect_tx(vis_full + vs, QT * kM);
+                        tma_load_3d(sVis + vs * QT * kM, &tma, vis_full + vs, kt * kM, un.s0, un.b);
                     }
                 }
             }
@@ -401,14 +491,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int kcount = 0, tcount = 0, qcount = 0;
             bool ok = true;
+            int4 rec_next = unit_rec<V41>(p, 0);
             for (int i = 0; ok; ++i) {
                 const int u = unit_of(i, p.num_units);
                 if (u == -2) break;
+                const int4 rec = rec_next;
+                rec_next = unit_rec<V41>(p, i + 1);
                 if (u < 0) continue;
-                const Unit un = make_unit<QT, V41>(p, u);
+                const Unit un = make_unit<QT, V41>(p, u, rec);
                 if (un.hi_t <= un.lo_t) continue;
-                if (!(ok = mbar_wait(q_full, qcount & 1, p.wait_ns))) break;
+                const int qb = qcount % NQB;
+                if (!(ok = mbar_wait(q_fullv(qb), (qcount / NQB) & 1, p.wait_ns))) break;
                 ++qcount;
+                // the second query buffer's descriptors: the start-address field (address/16,
+                // 14 bits) moves by the buffers' distance; shared addresses stay below 256 KB
+                const uint64_t qdelta = qb ? (uint64_t)((smem_u32(sQ1) - smem_u32(sQ)) >> 4) : 0ull;
                 tc_fence_after();
                 for (int kt = un.lo_t; kt < un.hi_t; ++kt) {
                     if (!tile_active<V41>(p, un, kt)) continue;
@@ -426,15 +523,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         uint64_t a = ad[0][k];
 #pragma unroll
                         for (int j = 1; j < kStages; ++j) a = st == j ? ad[j][k] : a;
-                        if (k < nk) umma_f16(d, a, bd[k], idesc, k > 0 ? 1u : 0u);
+                        if (k < nk) umma_f16(d, a, bd[k] + qdelta, idesc, k > 0 ? 1u : 0u);
                     }
                     umma_commit(k_empty + st);
                     umma_commit(acc_full + acc);
                 }
-                if (ok) umma_commit(q_empty);
+                if (ok) umma_commit(q_emptyv(qb));
             }
         }
-    } else if (warp < 2 + kEpiWarps) {
+    } else if (warp < 2 + EW) {
         // --------------------------------------------------------- epilogue
         const int etid = threadIdx.x - 64;
         const int quad = warp & 3;           // TMEM lane quadrant this warp may read
@@ -446,65 +543,99 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ntiles_all = (p.Skv + kM - 1) / kM;
         int tcount = 0, ucount = 0;
         bool ok = true;
+        int4 rec_next = unit_rec<V41>(p, 0);
+        // V4.1: accumulator columns of this warp (64 or 128), its whole queries, and
+        // its weight words per lane, held one unit ahead
+        constexpr int CPW = 4 * kN / EW, QW = CPW / H, WPER = H >= 2 ? 2 : 1;
+        constexpr int NWL = V41 ? CPW / WPER / 32 : 1;
+        const bool relu = p.act == 0;
+        uint32_t wreg[NWL];
+#pragma unroll
+        for (int k = 0; k < NWL; ++k)
+            wreg[k] = V41 ? v41_weight_word<H, QT>(p, unit_of(0, p.num_units), (half * CPW) / WPER + k * 32 + lane)
+                          : 0u;
         for (int i = 0; ok; ++i) {
             const int u = unit_of(i, p.num_units);
             if (u == -2) break;
+            const int4 rec = rec_next;
+            rec_next = unit_rec<V41>(p, i + 1);
             if (u < 0) continue;
-            const Unit un = make_unit<QT, V41>(p, u);
+            const Unit un = make_unit<QT, V41>(p, u, rec);
             if constexpr (V41) {
-                // bf16 weights of the query tile, two per word (one per word at H = 1)
-                constexpr int WPER = H >= 2 ? 2 : 1;
-                uint32_t* sWp = reinterpret_cast<uint32_t*>(sW);
-                named_bar_sync(kEpiBar, kEpiThreads);
-                for (int e = etid; e < kN / WPER; e += kEpiThreads) {
-                    const int ql = (WPER * e) / H, h = (WPER * e) % H, s = un.s0 + ql;
-                    uint32_t v = 0;
-                    if (s < p.S) {
-                        const uint16_t* wr = p.w16 + ((size_t)un.b * p.S + s) * H + h;
-                        v = WPER == 2 ? (uint32_t)wr[0] | ((uint32_t)wr[1] << 16) : (uint32_t)wr[0];
-                    }
-                    sWp[e] = v;
+                const int q0 = half * QW;  // this warp's first query within the tile
+                // the bf16 weights of this warp's queries (two per word) into the warp's
+                // own slot; they were loaded during the previous unit
+                uint32_t* const sWp = sWw + (warp - 2) * 64;
+                const int u1 = unit_of(i + 1, p.num_units);
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < NWL; ++k) {
+                    sWp[k * 32 + lane] = wreg[k];
+                    wreg[k] = v41_weight_word<H, QT>(p, u1, (half * CPW) / WPER + k * 32 + lane);
                 }
-                named_bar_sync(kEpiBar, kEpiThreads);
+                __syncwarp();
                 for (int kt = un.lo_t; kt < un.hi_t; ++kt) {
                     if (!tile_active<V41>(p, un, kt)) continue;  // written as -inf by the mask pass
                     const int t = kt * kM + row_t;
-                    const int acc = tcount & 1;
+                    const int acc = tcount & 1, vs = tcount % kVisStages;
+                    const uint32_t vph = (tcount / kVisStages) & 1;
+                    // without the ring: this thread's flags, read before the wait so that
+                    // their latency overlaps the tile's MMA (up to 8 queries a warp)
+                    constexpr int QF = QW <= 8 ? QW : 1;
+                    uint8_t vis[QF];
+#pragma unroll
+                    for (int j = 0; j < QF; ++j) {
+                        const int s = un.s0 + q0 + j;
+                        vis[j] = (!vis_tma && QW <= 8 && s < p.S && t < p.Skv)
+                                     ? p.allowed[((size_t)un.b * p.S + s) * p.Skv + t]
+                                     : (uint8_t)0;
+                    }
                     if (!(ok = mbar_wait(acc_full + acc, (tcount >> 1) & 1, p.wait_ns))) break;
                     ++tcount;
                     tc_fence_after();
+                    if (vis_tma && !(ok = mbar_wait(vis_full + vs, vph, p.wait_ns))) break;
+                    const uint8_t* sv = sVis + vs * QT * kM + row_t;
                     auto store16 = [&](int ql, float v) {
                         const int s = un.s0 + ql;
                         if (s >= p.S || t >= p.Skv) return;
                         const size_t o = ((size_t)un.b * p.S + s) * p.Skv + t;
+                        const bool visible = vis_tma     ? sv[ql * kM] != 0
+                                             : QW <= 8 ? vis[(ql - q0) % QF] != 0
+                                                       : p.allowed[o] != 0;
                         uint16_t bits = 0xFF80u;  // -inf
-                        if (p.allowed[o]) bits = (uint16_t)(__float_as_uint(bf16_round_f(v)) >> 16);
+                        if (visible) bits = (uint16_t)(__float_as_uint(bf16_round_f(v)) >> 16);
                         p.out16[o] = bits;
                     };
                     float run = 0.f;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < CPW / 32; ++c) {
                         uint32_t r[32];
-                        tmem_ld32(lane_addr + acc * kN + half * 128 + c * 32, r);
+                        tmem_ld32(lane_addr + acc * kN + half * CPW + c * 32, r);
                         tmem_ld_wait();
-                        if (c == 3) {
+                        if (c == CPW / 32 - 1) {
                             tc_fence_before();
                             __syncwarp();
                             if (lane == 0) mbar_arrive(acc_empty + acc);
                         }
-                        const uint32_t* wp = sWp + (half * 128 + c * 32) / WPER;
+                        const uint32_t* wp = sWp + (c * 32) / WPER;
                         if constexpr (H >= 32) {
-                            run += head_sum_v41<32>(r, 0, wp, p.act);
+                            run += relu ? head_sum_v41<32, true>(r, 0, wp) : head_sum_v41<32, false>(r, 0, wp);
                             if (((c + 1) * 32) % H == 0) {
-                                store16(half * QH + (c * 32) / H, run);
+                                store16(q0 + (c * 32) / H, run);
                                 run = 0.f;
                             }
                         } else {
 #pragma unroll
-                            for (int qq = 0; qq < 32 / H; ++qq)
-                                store16(half * QH + c * (32 / H) + qq,
-                                        head_sum_v41<H>(r, qq * H, wp + (qq * H) / WPER, p.act));
+                            for (int qq = 0; qq < 32 / H; ++qq) {
+                                const uint32_t* wq = wp + (qq * H) / WPER;
+                                store16(q0 + c * (32 / H) + qq, relu ? head_sum_v41<H, true>(r, qq * H, wq)
+                                                                     : head_sum_v41<H, false>(r, qq * H, wq));
+                            }
                         }
+                    }
+                    if (vis_tma) {  // this warp is done with the staged flags
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(vis_empty + vs);
                     }
                 }
                 continue;
@@ -595,6 +726,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             ++ucount;
         }
+    } else if constexpr (V41) {
+        // ---------------------------------------------------------- -inf fill
+        // The remaining warps write -inf over every block of the CTA's units that
+        // holds no visible pair, while the tensor-core sweep computes the others:
+        // each output element is written once, by this fill or by the epilogue.
+        constexpr int FT = kThreads - 64 - EWT;
+        const int ftid = threadIdx.x - 64 - EWT;
+        const bool vec = (p.Skv % 8) == 0 && (((uintptr_t)p.out16) & 15) == 0;
+        const uint4 ninf4 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+        int4 rec_next = unit_rec<true>(p, 0);
+        for (int i = 0;; ++i) {
+            const int u = unit_of(i, p.num_units);
+            if (u == -2) break;
+            const int4 rec = rec_next;
+            rec_next = unit_rec<true>(p, i + 1);
+            if (u < 0) continue;
+            const Unit un = make_unit<QT, true>(p, u, rec);
+            const int rows = min(QT, p.S - un.s0);
+            for (int r = 0; r < rows; ++r) {
+                uint16_t* o = p.out16 + ((size_t)un.b * p.S + un.s0 + r) * p.Skv;
+                if (vec) {
+                    for (int x = ftid * 8; x < p.Skv; x += FT * 8) {
+                        const int kt = x / kM;
+                        if (kt >= un.lo_t && kt < un.hi_t && tile_active<true>(p, un, kt)) continue;
+                        *reinterpret_cast<uint4*>(o + x) = ninf4;
+                    }
+                } else {
+                    for (int x = ftid; x < p.Skv; x += FT) {
+                        const int kt = x / kM;
+                        if (kt >= un.lo_t && kt < un.hi_t && tile_active<true>(p, un, kt)) continue;
+                        o[x] = 0xFF80u;
+                    }
+                }
+            }
+        }
     } else {
         // ------------------------------------------------------------ top-k
         // Group g selects rows g, g+G, g+2G, ... of this CTA's sequence of units
@@ -619,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     more = false;
                     break;
                 }
-                un = make_unit<QT, V41>(p, u);
+                un = make_unit<QT, V41>(p, u, make_int4(0, 0, 0, 0));  // V4 only
                 ++ucount;
                 ok = mbar_wait(rows_full + (ucount & 1), (ucount >> 1) & 1, p.wait_ns);
             }
@@ -683,26 +849,26 @@ static int encode_maps(const ScoreLaunch& a, CUtensorMap* mq, CUtensorMap* mk) {
 
 template <int H, bool V41>
 static cudaError_t launch_h(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
-                            int smem, int grid) {
+                            const CUtensorMap& ma, int smem, int grid) {
     auto kern = score_fwd_kernel<H, V41>;
     cudaError_t e = set_smem_attr((const void*)kern, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, a.p);
+    kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, ma, a.p);
     return cudaGetLastError();
 }
 
 template <bool V41>
 static cudaError_t launch_any(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
-                              int smem, int grid) {
+                              const CUtensorMap& ma, int smem, int grid) {
     switch (a.p.H) {
-        case 1: return launch_h<1, V41>(a, mq, mk, smem, grid);
-        case 2: return launch_h<2, V41>(a, mq, mk, smem, grid);
-        case 4: return launch_h<4, V41>(a, mq, mk, smem, grid);
-        case 8: return launch_h<8, V41>(a, mq, mk, smem, grid);
-        case 16: return launch_h<16, V41>(a, mq, mk, smem, grid);
-        case 32: return launch_h<32, V41>(a, mq, mk, smem, grid);
-        case 64: return launch_h<64, V41>(a, mq, mk, smem, grid);
-        case 128: return launch_h<128, V41>(a, mq, mk, smem, grid);
+        case 1: return launch_h<1, V41>(a, mq, mk, ma, smem, grid);
+        case 2: return launch_h<2, V41>(a, mq, mk, ma, smem, grid);
+        case 4: return launch_h<4, V41>(a, mq, mk, ma, smem, grid);
+        case 8: return launch_h<8, V41>(a, mq, mk, ma, smem, grid);
+        case 16: return launch_h<16, V41>(a, mq, mk, ma, smem, grid);
+        case 32: return launch_h<32, V41>(a, mq, mk, ma, smem, grid);
+        case 64: return launch_h<64, V41>(a, mq, mk, ma, smem, grid);
+        case 128: return launch_h<128, V41>(a, mq, mk, ma, smem, grid);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -734,7 +900,9 @@ int score_fwd_launch(ScoreLaunch& a) {
     int smem = (int)smem_layout(p.D).total;
     if (smem < 120 * 1024) smem = 120 * 1024;
     if (p.H < 1 || p.H > 128 || (p.H & (p.H - 1))) return -2;
-    const cudaError_t e = launch_any<false>(a, mq, mk, smem, grid);
+    CUtensorMap unused;
+    memset(&unused, 0, sizeof unused);
+    const cudaError_t e = launch_any<false>(a, mq, mk, unused, smem, grid);
     a.launched = grid;
     return e == cudaSuccess ? 0 : -1;
 }
@@ -771,9 +939,22 @@ int score_v41_launch(ScoreLaunch& a) {
     cuuint32_t kbox[3] = {(cuuint32_t)KB, (cuuint32_t)kM, 1};
     if (encode_tiled(&mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)a.k, kdim, kstr, kbox, es, sw))
         return -1;
+    // visibility flags by TMA: rows of `allowed` 16-byte aligned, QT <= 32 (H >= 8)
+    CUtensorMap ma;
+    memset(&ma, 0, sizeof ma);
+    p.vis_tma = 0;
+    if (QT <= 32 && (p.Skv % 16) == 0 && ((uintptr_t)p.allowed & 15) == 0) {
+        cuuint64_t adim[3] = {(cuuint64_t)p.Skv, (cuuint64_t)p.S, (cuuint64_t)B};
+        cuuint64_t astr[2] = {(cuuint64_t)p.Skv, (cuuint64_t)p.S * p.Skv};
+        cuuint32_t abox[3] = {(cuuint32_t)kM, (cuuint32_t)QT, 1};
+        if (encode_tiled(&ma, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, (void*)p.allowed, adim, astr, abox, es,
+                         CU_TENSOR_MAP_SWIZZLE_NONE))
+            return -1;
+        p.vis_tma = 1;
+    }
     int smem = (int)smem_layout(p.D).total;
     if (smem < 120 * 1024) smem = 120 * 1024;
-    const cudaError_t e = launch_any<true>(a, mq, mk, smem, grid);
+    const cudaError_t e = launch_any<true>(a, mq, mk, ma, smem, grid);
     a.launched = grid;
     return e == cudaSuccess ? 0 : -1;
 }

@@ -2,9 +2,9 @@
 // indexer_scores: boolean `allowed` [batch, local_sequence, global_compressed]).
 //
 // One streaming read of `allowed` decides, for every (query tile, 128-key tile)
-// block, whether any pair in it is visible.  Blocks with no visible pair get
-// their scores written here as -inf, so the tensor-core pass touches only
-// blocks with work and every output element is written exactly once.
+// block, whether any pair in it is visible, and for every query tile the range
+// of key tiles that holds its visible pairs.  The scoring kernel then computes
+// the blocks with a visible pair and writes -inf over the others.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -15,19 +15,40 @@ namespace lidx {
 
 constexpr int kMaskThreads = 256;
 
+// The unit's record: key tiles [first, last] hold every visible pair, and bit j
+// of the 64-bit mask is the tile map's entry for key tile first + j (one warp;
+// the map row was written by this block before the caller's barrier).
+__device__ __forceinline__ void write_unit_record(const uint8_t* map, int first, int last, int lane,
+                                                  int4* rec) {
+    int4 r = make_int4(0, 0, 0, 0);
+    if (last >= 0) {
+        const int j0 = first + lane, j1 = first + 32 + lane;
+        const uint32_t m0 = __ballot_sync(0xffffffffu, j0 <= last && map[j0] != 0);
+        const uint32_t m1 = __ballot_sync(0xffffffffu, j1 <= last && map[j1] != 0);
+        r = make_int4(first, last + 1, (int)m0, (int)m1);
+    }
+    if (lane == 0) *rec = r;
+}
+
 // Grid-stride over (b, query tile); each warp takes key tiles in turn.  Lane l
 // covers keys [kt*128 + 4l, kt*128 + 4l + 4) of every row of the tile.
 __global__ void __launch_bounds__(kMaskThreads)
-    v41_mask_kernel(const uint8_t* __restrict__ allowed, uint16_t* __restrict__ out,
-                    uint8_t* __restrict__ tilemap, int B, int S, int Skv, int QT, int qtiles,
-                    int ntk) {
+    v41_mask_kernel(const uint8_t* __restrict__ allowed, uint8_t* __restrict__ tilemap, int4* __restrict__ urec, int B, int S, int Skv,
+                    int QT, int qtiles, int ntk) {
+    __shared__ int s_first, s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int NW = kMaskThreads / 32;
-    const bool vec = (Skv & 3) == 0;  // rows start 4-byte aligned: word loads, 8-byte stores
+    const bool vec = (Skv & 3) == 0;  // rows start 4-byte aligned: word loads
     const int units = B * qtiles;
     for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const int b = unit / qtiles, qt = unit % qtiles, s0 = qt * QT;
         const int rows = min(QT, S - s0);
+        __syncthreads();  // the previous unit's range is written out
+        if (threadIdx.x == 0) {
+            s_first = ntk;
+            s_last = -1;
+        }
+        __syncthreads();
         for (int kt = warp; kt < ntk; kt += NW) {
             const int t0 = kt * 128 + lane * 4;
             uint32_t any = 0;
@@ -42,20 +63,16 @@ __global__ void __launch_bounds__(kMaskThreads)
                 }
             }
             const bool active = __any_sync(0xffffffffu, any != 0);
-            if (lane == 0) tilemap[(size_t)unit * ntk + kt] = active ? 1 : 0;
-            if (!active) {
-                for (int r = 0; r < rows; ++r) {
-                    uint16_t* o = out + ((size_t)b * S + s0 + r) * Skv;
-                    if (vec && t0 + 3 < Skv) {
-                        *reinterpret_cast<uint2*>(o + t0) = make_uint2(0xFF80FF80u, 0xFF80FF80u);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            if (t0 + j < Skv) o[t0 + j] = 0xFF80u;
-                    }
+            if (lane == 0) {
+                tilemap[(size_t)unit * ntk + kt] = active ? 1 : 0;
+                if (active) {
+                    atomicMin(&s_first, kt);
+                    atomicMax(&s_last, kt);
                 }
             }
         }
+        __syncthreads();
+        if (warp == 0) write_unit_record(tilemap + (size_t)unit * ntk, s_first, s_last, lane, urec + unit);
     }
 }
 
@@ -63,9 +80,9 @@ __global__ void __launch_bounds__(kMaskThreads)
 // reads 16 flags of up to four rows at once, so a warp keeps 2 KB of `allowed`
 // in flight and covers four key tiles (8 lanes each) per step.
 __global__ void __launch_bounds__(kMaskThreads)
-    v41_mask_kernel16(const uint8_t* __restrict__ allowed, uint16_t* __restrict__ out,
-                      uint8_t* __restrict__ tilemap, int B, int S, int Skv, int QT, int qtiles,
-                      int ntk) {
+    v41_mask_kernel16(const uint8_t* __restrict__ allowed, uint8_t* __restrict__ tilemap, int4* __restrict__ urec, int B, int S,
+                      int Skv, int QT, int qtiles, int ntk) {
+    __shared__ int s_first, s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int NW = kMaskThreads / 32;
     const int units = B * qtiles;
@@ -73,6 +90,12 @@ __global__ void __launch_bounds__(kMaskThreads)
     for (int unit = blockIdx.x; unit < units; unit += gridDim.x) {
         const int b = unit / qtiles, qt = unit % qtiles, s0 = qt * QT;
         const int rows = min(QT, S - s0);
+        __syncthreads();  // the previous unit's range is written out
+        if (threadIdx.x == 0) {
+            s_first = ntk;
+            s_last = -1;
+        }
+        __syncthreads();
         for (int ch = warp; ch < nchunks; ch += NW) {
             const int t0 = ch * 512 + lane * 16;
             const bool in = t0 < Skv;  // Skv % 16 == 0: all 16 keys inside or none
@@ -99,34 +122,33 @@ __global__ void __launch_bounds__(kMaskThreads)
             any |= __shfl_xor_sync(0xffffffffu, any, 2);
             any |= __shfl_xor_sync(0xffffffffu, any, 4);
             const int kt = ch * 4 + (lane >> 3);
-            if ((lane & 7) == 0 && kt < ntk) tilemap[(size_t)unit * ntk + kt] = any ? 1 : 0;
-            if (!any && in) {
-                const uint4 ninf = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-                uint16_t* o = out + ((size_t)b * S + s0) * Skv + t0;
-                for (int r2 = 0; r2 < rows; ++r2) {
-                    uint4* d = reinterpret_cast<uint4*>(o + (size_t)r2 * Skv);
-                    d[0] = ninf;
-                    d[1] = ninf;
+            if ((lane & 7) == 0 && kt < ntk) {
+                tilemap[(size_t)unit * ntk + kt] = any ? 1 : 0;
+                if (any) {
+                    atomicMin(&s_first, kt);
+                    atomicMax(&s_last, kt);
                 }
             }
         }
+        __syncthreads();
+        if (warp == 0) write_unit_record(tilemap + (size_t)unit * ntk, s_first, s_last, lane, urec + unit);
     }
 }
 
-cudaError_t v41_mask_launch(const uint8_t* allowed, uint16_t* out, uint8_t* tilemap, int B, int S,
-                            int Skv, int QT, cudaStream_t stream) {
+cudaError_t v41_mask_launch(const uint8_t* allowed, uint8_t* tilemap, int4* urec, int B, int S, int Skv,
+                            int QT, cudaStream_t stream) {
     const int qtiles = (S + QT - 1) / QT, ntk = (Skv + 127) / 128;
     const int64_t units = (int64_t)B * qtiles;
     if (units == 0 || ntk == 0) return cudaSuccess;
     const int sms = current_sms();
     int64_t grid = (int64_t)sms * 8;
     if (grid > units) grid = units;
-    if ((Skv & 15) == 0 && ((((uintptr_t)allowed) | ((uintptr_t)out)) & 15) == 0)
-        v41_mask_kernel16<<<(unsigned)grid, kMaskThreads, 0, stream>>>(allowed, out, tilemap, B, S,
-                                                                       Skv, QT, qtiles, ntk);
+    if ((Skv & 15) == 0 && (((uintptr_t)allowed) & 15) == 0)
+        v41_mask_kernel16<<<(unsigned)grid, kMaskThreads, 0, stream>>>(allowed, tilemap, urec, B, S, Skv,
+                                                                       QT, qtiles, ntk);
     else
-        v41_mask_kernel<<<(unsigned)grid, kMaskThreads, 0, stream>>>(allowed, out, tilemap, B, S, Skv,
-                                                                     QT, qtiles, ntk);
+        v41_mask_kernel<<<(unsigned)grid, kMaskThreads, 0, stream>>>(allowed, tilemap, urec, B, S, Skv, QT,
+                                                                     qtiles, ntk);
     return cudaGetLastError();
 }
 

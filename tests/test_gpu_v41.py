@@ -121,6 +121,27 @@ def test_shapes_random_visibility(B, S, Skv, H, D, density):
     check(gi, oracle.scores_v41_rows(q, k, w, allowed, act="identity"), allowed, bound=bnd)
 
 
+@pytest.mark.parametrize("Skv", [9000, 8464])
+def test_key_range_beyond_64_tiles(Skv):
+    """A query tile whose visible pairs span more than 64 key tiles, with blocks
+    of no visible pair inside the span on both sides of the 64th tile (9000: the
+    word-load visibility pass; 8464: the 16-byte one)."""
+    B, S, H, D = 1, 40, 16, 32
+    g = np.random.default_rng(Skv)
+    q = workloads.to_bf16(g.standard_normal((B, S, H, D)).astype(np.float32) / np.sqrt(D))
+    k = workloads.to_bf16(g.standard_normal((B, Skv, D)).astype(np.float32) / np.sqrt(D))
+    w = workloads.to_bf16(g.standard_normal((B, S, H)).astype(np.float32) / np.sqrt(H))
+    ntk = (Skv + 127) // 128
+    tiles = [1, 2, 40, 63, 64, 66, ntk - 1]
+    al = np.zeros((B, S, Skv), dtype=bool)
+    for t in tiles:
+        lo, hi = t * 128, min(t * 128 + 128, Skv)
+        al[:, :, lo:hi] = g.random((B, S, hi - lo)) < 0.3
+    allowed = torch.from_numpy(al)
+    got = run(q, k, w, allowed).reshape(B * S, Skv)
+    check(got, oracle.scores_v41_rows(q, k, w, allowed), allowed, bound=flip_bound(q, k, w))
+
+
 def test_all_false_and_all_true():
     g = np.random.default_rng(8)
     B, S, Skv, H, D = 1, 50, 200, 8, 32
