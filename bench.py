@@ -243,11 +243,23 @@ def time_steps(fn, steps, stream):
 
 
 def _median_ms(fn, stream, reps, flush=None):
+    """Median device time of one call.  The L2 flush (a 256 MB write, tens of
+    microseconds on the device) is enqueued on the same stream first, so that
+    the call's launches are queued behind it and the events bracket device work
+    only, not the host's launch latency."""
     ts = []
     for _ in range(reps):
-        if flush is not None:
-            flush.zero_()
-        ts.append(time_steps(fn, 1, stream))
+        torch.cuda.synchronize()
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            if flush is not None:
+                flush.zero_()
+            start.record(stream)
+            fn()
+            end.record(stream)
+        end.synchronize()
+        ts.append(start.elapsed_time(end))
     return statistics.median(ts)
 
 

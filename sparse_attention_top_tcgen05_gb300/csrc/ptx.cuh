@@ -95,6 +95,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     return true;
 }
 
+// ------------------------------------------------- programmatic launch
+// Lets the next kernel on the stream (launched with programmatic stream
+// serialisation) start its prologue while this grid still runs.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Waits until the grids this one depends on have completed and their memory
+// is visible; returns at once when the launch had no such dependency.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // --------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");

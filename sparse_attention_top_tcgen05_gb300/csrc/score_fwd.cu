@@ -411,6 +411,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // V4.1: the visibility records come from the preceding pass, which may still
+    // be finishing when this grid starts (programmatic launch)
+    if constexpr (V41) griddep_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -744,21 +747,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (u < 0) continue;
             const Unit un = make_unit<QT, true>(p, u, rec);
             const int rows = min(QT, p.S - un.s0);
-            for (int r = 0; r < rows; ++r) {
-                uint16_t* o = p.out16 + ((size_t)un.b * p.S + un.s0 + r) * p.Skv;
-                if (vec) {
-                    for (int x = ftid * 8; x < p.Skv; x += FT * 8) {
-                        const int kt = x / kM;
-                        if (kt >= un.lo_t && kt < un.hi_t && tile_active<true>(p, un, kt)) continue;
-                        *reinterpret_cast<uint4*>(o + x) = ninf4;
-                    }
-                } else {
-                    for (int x = ftid; x < p.Skv; x += FT) {
-                        const int kt = x / kM;
-                        if (kt >= un.lo_t && kt < un.hi_t && tile_active<true>(p, un, kt)) continue;
-                        o[x] = 0xFF80u;
-                    }
+            // keys [a, b) of every row of the unit; a and b multiples of 8 when vec
+            auto fill = [&](int a, int b) {
+                for (int r = 0; r < rows; ++r) {
+                    uint16_t* o = p.out16 + ((size_t)un.b * p.S + un.s0 + r) * p.Skv;
+                    if (vec)
+                        for (int x = a + ftid * 8; x < b; x += FT * 8) *reinterpret_cast<uint4*>(o + x) = ninf4;
+                    else
+                        for (int x = a + ftid; x < b; x += FT) o[x] = 0xFF80u;
                 }
+            };
+            // the key tiles before and after the unit's range, then the empty tiles inside it
+            const int lo_k = un.lo_t * kM, hi_k = min(un.hi_t * kM, p.Skv);
+            if (un.hi_t > un.lo_t) {
+                fill(0, lo_k);
+                fill(hi_k, p.Skv);
+                for (int kt = un.lo_t + 1; kt < un.hi_t - 1; ++kt)
+                    if (!tile_active<true>(p, un, kt)) fill(kt * kM, kt * kM + kM);
+            } else {
+                fill(0, p.Skv);
             }
         }
     } else {
@@ -853,8 +860,24 @@ static cudaError_t launch_h(const ScoreLaunch& a, const CUtensorMap& mq, const C
     auto kern = score_fwd_kernel<H, V41>;
     cudaError_t e = set_smem_attr((const void*)kern, smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, ma, a.p);
-    return cudaGetLastError();
+    if constexpr (!V41) {
+        kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, ma, a.p);
+        return cudaGetLastError();
+    }
+    // V4.1 follows its visibility pass on the stream: launched so that its
+    // set-up overlaps the end of that pass (it waits for the records itself)
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = (cudaStream_t)a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, mq, mk, ma, a.p);
 }
 
 template <bool V41>

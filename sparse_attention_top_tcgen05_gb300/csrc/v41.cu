@@ -37,6 +37,7 @@ __global__ void __launch_bounds__(kMaskThreads)
                     int QT, int qtiles, int ntk) {
     __shared__ int s_first, s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_launch_dependents();  // the scoring kernel may start its set-up now
     constexpr int NW = kMaskThreads / 32;
     const bool vec = (Skv & 3) == 0;  // rows start 4-byte aligned: word loads
     const int units = B * qtiles;
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kMaskThreads)
                       int Skv, int QT, int qtiles, int ntk) {
     __shared__ int s_first, s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    griddep_launch_dependents();  // the scoring kernel may start its set-up now
     constexpr int NW = kMaskThreads / 32;
     const int units = B * qtiles;
     const int nchunks = (ntk + 3) / 4;  // 512-key chunks
