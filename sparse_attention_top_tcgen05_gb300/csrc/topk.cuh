@@ -48,6 +48,7 @@ constexpr int kTopkCap = 4096;       // members of one window held in shared mem
 constexpr int kTopkSmall = 64;       // buckets up to this size are ranked pairwise
 constexpr int kTopkWarpSort = 512;   // larger buckets up to this size: one warp sorts each
 constexpr int kTopkMaxKeys = 65536;  // visible span of a row (16-bit candidate offsets)
+constexpr int kTopkShort = 128;      // rows up to this span: one warp sorts the row in registers
 // Pending refined items are disjoint.  Those refined because they exceed a
 // window (> kTopkCap members) number at most 15; those refined by choice (a
 // bucket of more than kTopkWarpSort unequal members) at most kTopkStackOpt.
@@ -677,6 +678,78 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
     }
 }
 
+// Bitonic sort, descending, of 32*E 64-bit keys held by one warp: element
+// k*32 + lane lives in x[k] of that lane.
+template <int E>
+__device__ __forceinline__ void warp_bitonic_desc64(uint64_t (&x)[E], int lane) {
+    constexpr int N = 32 * E;
+#pragma unroll
+    for (int sz = 2; sz <= N; sz <<= 1) {
+#pragma unroll
+        for (int d = sz >> 1; d > 0; d >>= 1) {
+            if (d >= 32) {  // partner in another register of this lane
+                const int kd = d / 32;
+#pragma unroll
+                for (int k = 0; k < E; ++k) {
+                    if (k & kd) continue;
+                    const bool desc = ((k * 32 + lane) & sz) == 0;
+                    const uint64_t a = x[k], b = x[k | kd];
+                    const bool sw = desc ? a < b : a > b;
+                    x[k] = sw ? b : a;
+                    x[k | kd] = sw ? a : b;
+                }
+            } else {  // partner in this register of lane ^ d
+#pragma unroll
+                for (int k = 0; k < E; ++k) {
+                    const int i = k * 32 + lane;
+                    const uint64_t y = __shfl_xor_sync(0xffffffffu, x[k], d);
+                    const bool keep_max = (((i & sz) == 0) == ((i & d) == 0));
+                    x[k] = keep_max ? (x[k] > y ? x[k] : y) : (x[k] < y ? x[k] : y);
+                }
+            }
+        }
+    }
+}
+
+// A short row (n <= 32*E) selected by one warp: each entry becomes the key
+// (order key of the value, then the complement of its offset), so that one
+// descending sort gives the output order (equal values by ascending key).
+// Scores are copied from the row.  With SKIP_NINF, -inf entries are not emitted.
+template <int E, bool SKIP_NINF, class T>
+__device__ void warp_topk_short(const T* r, int n, int lo, int topk, int32_t* out_idx, T* out_sc,
+                                int lane) {
+    const float ninf = __int_as_float(0xff800000);
+    uint64_t x[E];
+    int valid = 0;
+#pragma unroll
+    for (int k = 0; k < E; ++k) {
+        const int j = k * 32 + lane;
+        x[k] = 0ull;  // padding sorts after every entry
+        bool ok = false;
+        if (j < n) {
+            const float v = topk_to_f<T>(r[j]);
+            ok = !SKIP_NINF || v > ninf;
+            x[k] = ((uint64_t)topk_okey(v) << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)j);
+        }
+        valid += __popc(__ballot_sync(0xffffffffu, ok));
+    }
+    warp_bitonic_desc64<E>(x, lane);
+    const int sel = valid < topk ? valid : topk;
+#pragma unroll
+    for (int k = 0; k < E; ++k) {
+        const int i = k * 32 + lane;
+        if (i < sel) {
+            const int j = (int)(0xFFFFFFFFu - (uint32_t)x[k]);
+            out_idx[i] = lo + j;
+            out_sc[i] = r[j];
+        }
+    }
+    for (int i = sel + lane; i < topk; i += 32) {
+        out_idx[i] = -1;
+        out_sc[i] = topk_from_f<T>(ninf);
+    }
+}
+
 // Selects the top `topk` of row[lo..hi) into out_idx/out_sc.  All NT threads
 // of the group must call it with identical scalar arguments, after a group
 // barrier that ends any earlier use of `sm`; hi - lo must not exceed
@@ -688,6 +761,18 @@ __device__ void row_topk(const T* row, int lo, int hi, int topk, int32_t* out_id
     const int n = hi > lo ? hi - lo : 0;
     const float ninf = __int_as_float(0xff800000), pinf = __int_as_float(0x7f800000);
     const T* r = row + lo;
+    if (n <= kTopkShort) {  // one warp sorts the row in registers
+        if (tid < 32) {
+            if (n <= 32)
+                warp_topk_short<1, SKIP_NINF, T>(r, n, lo, topk, out_idx, out_sc, tid);
+            else if (n <= 64)
+                warp_topk_short<2, SKIP_NINF, T>(r, n, lo, topk, out_idx, out_sc, tid);
+            else
+                warp_topk_short<4, SKIP_NINF, T>(r, n, lo, topk, out_idx, out_sc, tid);
+        }
+        named_bar_sync(bar_id, NT);  // the group moves on together
+        return;
+    }
 
     // 1. min, max and number of visible scores
     float vmax = ninf, vmin = pinf;
