@@ -282,134 +282,144 @@ def selection_rows(kind, rows, Skv, seed=0):
     return torch.from_numpy(x.astype(np.float32))
 
 
-def side_workloads(lidx, pk):
-    """Short measurements of the other workloads' kernels (not the headline)."""
+def side_workloads(lidx, pk, names=None):
+    """Short measurements of the other workloads' kernels (not the headline);
+    ``names`` picks a subset of tiny, c4_fwd, v41_packed, selection, bwd."""
     out = {}
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
 
-    # tiny workload: latency of one call (logits materialised, then top-k)
-    wl = workloads.WORKLOADS["tiny"]
-    q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
-    idx = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.int32, device="cuda")
-    sc = torch.empty_like(idx, dtype=torch.float32)
-    lg = torch.empty(wl.B, wl.S, wl.Skv, dtype=torch.float32, device="cuda")
-    fn = lambda: lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk, materialise_logits=True,
-                                       out=(idx, sc, lg))
-    for _ in range(10):
-        fn()
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(200):
-        fn()
-    torch.cuda.synchronize()
-    host_us = (time.perf_counter() - t0) / 200 * 1e6
-    out["tiny"] = {"us_per_call": 1e3 * time_steps(fn, 200, stream), "host_us_per_call": host_us,
-                   "launches": 1, "note": "back-to-back calls, L2 warm; host_us includes the "
-                   "Python binding and the C ABI's argument checks"}
-    del q, k, w, idx, sc, lg
+    def _tiny():
+        # tiny workload: latency of one call (logits materialised, then top-k)
+        wl = workloads.WORKLOADS["tiny"]
+        q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
+        idx = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.int32, device="cuda")
+        sc = torch.empty_like(idx, dtype=torch.float32)
+        lg = torch.empty(wl.B, wl.S, wl.Skv, dtype=torch.float32, device="cuda")
+        fn = lambda: lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk, materialise_logits=True,
+                                           out=(idx, sc, lg))
+        for _ in range(10):
+            fn()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(200):
+            fn()
+        torch.cuda.synchronize()
+        host_us = (time.perf_counter() - t0) / 200 * 1e6
+        out["tiny"] = {"us_per_call": 1e3 * time_steps(fn, 200, stream), "host_us_per_call": host_us,
+                       "launches": 1, "note": "back-to-back calls, L2 warm; host_us includes the "
+                       "Python binding and the C ABI's argument checks"}
+        del q, k, w, idx, sc, lg
 
-    wl = workloads.WORKLOADS["c4_fwd"]
-    q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
-    idx = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.int32, device="cuda")
-    sc = torch.empty_like(idx, dtype=torch.float32)
-    lg = torch.empty(wl.B, wl.S, wl.Skv, dtype=torch.float32, device="cuda")
-    fn = lambda: lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk, materialise_logits=True,
-                                       out=(idx, sc, lg))
-    for _ in range(3):
-        fn()
-    ms = _median_ms(fn, stream, 10, flush)
-    pairs = visible_pairs(wl.S, wl.Skv, wl.ratio, wl.B)
-    fl = pairs * 2.0 * wl.H * wl.D
-    alg_bytes = q.numel() * 2 + k.numel() * 2 + w.numel() * 4 + lg.numel() * 4 + idx.numel() * 8
-    out["c4_fwd"] = {"ms": ms, "tflops": fl / ms / 1e9, "rows_per_s": wl.B * wl.S / ms * 1e3,
-                     "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
-                     "hbm_gbs": alg_bytes / ms / 1e6, "hbm_frac": alg_bytes / ms / 1e6 / pk["hbm_gbs"],
-                     "l2": "256 MB flush before each launch"}
-    # the same layer with the previous selection given (no selection; scores of those keys)
-    given = idx.clone()
-    ws = torch.empty(lidx.lidx_workspace_bytes(lidx.OP_INDEXER_FWD, wl.B, wl.S, wl.Skv, wl.H, wl.D,
-                                               wl.topk), dtype=torch.uint8, device="cuda")
-    fn = lambda: lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk, topk_indices=given,
-                                       out=(idx, sc, None), workspace=ws)
-    for _ in range(3):
-        fn()
-    ms = _median_ms(fn, stream, 10, flush)
-    out["c4_fwd_given_indices"] = {"ms": ms, "tflops": fl / ms / 1e9,
-                                   "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
-                                   "note": "topk_indices given: same tensor-core sweep, the "
-                                   "selection replaced by a gather", "l2": "256 MB flush"}
-    del q, k, w, idx, sc, lg, given, ws
-
-    # V4.1 packed documents: HBM-bound (q, allowed read; bf16 scores written)
-    wl = workloads.WORKLOADS["v41_packed"]
-    q, k, w, allowed = [t.cuda() for t in workloads.v41_inputs(wl, 0)]
-    out16 = torch.empty(wl.B, wl.S, wl.Skv, dtype=torch.bfloat16, device="cuda")
-    wsb = lidx.lidx_workspace_bytes(lidx.OP_SCORES_V41, wl.B, wl.S, wl.Skv, wl.H, wl.D)
-    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
-    fn = lambda: lidx.lidx_indexer_scores_v41(q, k, w, allowed, out=out16, workspace=ws)
-    for _ in range(3):
-        fn()
-    ms = _median_ms(fn, stream, 10, flush)
-    vis = int(allowed.sum().item())
-    alg_bytes = (q.numel() * 2 + k.numel() * 2 + w.numel() * 2 + allowed.numel() + out16.numel() * 2)
-    out["v41_packed"] = {"ms": ms, "hbm_gbs": alg_bytes / ms / 1e6,
-                         "hbm_frac": alg_bytes / ms / 1e6 / pk["hbm_gbs"],
-                         "algorithmic_bytes": alg_bytes, "visible_pairs": vis,
-                         "visible_pair_tflops": vis * 2.0 * wl.H * wl.D / ms / 1e9,
-                         "launches": 2, "l2": "256 MB flush before each call"}
-    tidx = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.int32, device="cuda")
-    tsc = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.bfloat16, device="cuda")
-    wsb = lidx.lidx_workspace_bytes(lidx.OP_TOPK_V41, wl.B, wl.S, wl.Skv, wl.H, wl.D, wl.topk, True)
-    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
-    fn = lambda: lidx.lidx_indexer_topk_v41(q, k, w, allowed, wl.topk, out=(out16, tidx, tsc),
-                                            workspace=ws)
-    for _ in range(3):
-        fn()
-    ms2 = _median_ms(fn, stream, 10, flush)
-    out["v41_packed_topk"] = {"ms": ms2, "topk": wl.topk, "selection_ms": ms2 - ms,
-                              "rows_per_s": wl.B * wl.S / ms2 * 1e3, "launches": 3,
-                              "l2": "256 MB flush before each call"}
-    del q, k, w, allowed, out16, ws, tidx, tsc
-
-    # selection alone on adversarial rows: time of a tie-heavy row against a normal one
-    rows, Skv, topk = 4096, 4096, 2048
-    sel = {}
-    for kind in ("normal", "ties", "const", "zero_pad", "two_values"):
-        x = selection_rows(kind, rows, Skv).cuda()
-        oi = torch.empty(rows, topk, dtype=torch.int32, device="cuda")
-        os_ = torch.empty(rows, topk, dtype=torch.float32, device="cuda")
-        fn = lambda: lidx.lidx_topk_rows(x, topk, out=(oi, os_))
+    def _c4_fwd():
+        wl = workloads.WORKLOADS["c4_fwd"]
+        q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
+        idx = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.int32, device="cuda")
+        sc = torch.empty_like(idx, dtype=torch.float32)
+        lg = torch.empty(wl.B, wl.S, wl.Skv, dtype=torch.float32, device="cuda")
+        fn = lambda: lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk, materialise_logits=True,
+                                           out=(idx, sc, lg))
         for _ in range(3):
             fn()
-        sel[kind] = time_steps(fn, 10, stream)
-        del x, oi, os_
-    out["selection"] = {"rows": rows, "Skv": Skv, "topk": topk, "ms": sel,
-                        "worst_over_normal": max(sel.values()) / sel["normal"],
-                        "kernel": "topk_rows_kernel (standalone selection, 256 threads per row)"}
+        ms = _median_ms(fn, stream, 10, flush)
+        pairs = visible_pairs(wl.S, wl.Skv, wl.ratio, wl.B)
+        fl = pairs * 2.0 * wl.H * wl.D
+        alg_bytes = q.numel() * 2 + k.numel() * 2 + w.numel() * 4 + lg.numel() * 4 + idx.numel() * 8
+        out["c4_fwd"] = {"ms": ms, "tflops": fl / ms / 1e9, "rows_per_s": wl.B * wl.S / ms * 1e3,
+                         "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
+                         "hbm_gbs": alg_bytes / ms / 1e6, "hbm_frac": alg_bytes / ms / 1e6 / pk["hbm_gbs"],
+                         "l2": "256 MB flush before each launch"}
+        # the same layer with the previous selection given (no selection; scores of those keys)
+        given = idx.clone()
+        ws = torch.empty(lidx.lidx_workspace_bytes(lidx.OP_INDEXER_FWD, wl.B, wl.S, wl.Skv, wl.H, wl.D,
+                                                   wl.topk), dtype=torch.uint8, device="cuda")
+        fn = lambda: lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk, topk_indices=given,
+                                           out=(idx, sc, None), workspace=ws)
+        for _ in range(3):
+            fn()
+        ms = _median_ms(fn, stream, 10, flush)
+        out["c4_fwd_given_indices"] = {"ms": ms, "tflops": fl / ms / 1e9,
+                                       "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"],
+                                       "note": "topk_indices given: same tensor-core sweep, the "
+                                       "selection replaced by a gather", "l2": "256 MB flush"}
+        del q, k, w, idx, sc, lg, given, ws
 
-    # backward through the selected entries (selection: the forward's own top-k)
-    wl = workloads.WORKLOADS["bwd"]
-    q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
-    idx, _, _ = lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk)
-    grad = workloads.grad_scores(wl.B, wl.S, wl.topk, 0).cuda()
-    outs = (torch.empty(wl.S, wl.B, wl.H, wl.D, device="cuda"), torch.empty(wl.Skv, wl.B, wl.D, device="cuda"),
-            torch.empty(wl.S, wl.B, wl.H, device="cuda"))
-    wsb = lidx.lidx_workspace_bytes(lidx.OP_INDEXER_BWD, wl.B, wl.S, wl.Skv, wl.H, wl.D, wl.topk)
-    ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
-    fn = lambda: lidx.lidx_indexer_bwd(q, k, w, idx, grad, wl.ratio, out=outs, workspace=ws)
-    for _ in range(2):
-        fn()
-    ms = time_steps(fn, 10, stream)
-    nsel = int((idx >= 0).sum().item())
-    fl = nsel * 6.0 * wl.H * wl.D
-    out["bwd"] = {"ms": ms, "selected_pairs": nsel, "tflops": fl / ms / 1e9,
-                  "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"], "kernel": BWD_KERNEL,
-                  "launches": 4, "algorithmic": "6*H*D FLOP per selected pair",
-                  "workspace_bytes": wsb}
-    del q, k, w, idx, grad, outs, ws
+    def _v41_packed():
+        # V4.1 packed documents: HBM-bound (q, allowed read; bf16 scores written)
+        wl = workloads.WORKLOADS["v41_packed"]
+        q, k, w, allowed = [t.cuda() for t in workloads.v41_inputs(wl, 0)]
+        out16 = torch.empty(wl.B, wl.S, wl.Skv, dtype=torch.bfloat16, device="cuda")
+        wsb = lidx.lidx_workspace_bytes(lidx.OP_SCORES_V41, wl.B, wl.S, wl.Skv, wl.H, wl.D)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+        fn = lambda: lidx.lidx_indexer_scores_v41(q, k, w, allowed, out=out16, workspace=ws)
+        for _ in range(3):
+            fn()
+        ms = _median_ms(fn, stream, 10, flush)
+        vis = int(allowed.sum().item())
+        alg_bytes = (q.numel() * 2 + k.numel() * 2 + w.numel() * 2 + allowed.numel() + out16.numel() * 2)
+        out["v41_packed"] = {"ms": ms, "hbm_gbs": alg_bytes / ms / 1e6,
+                             "hbm_frac": alg_bytes / ms / 1e6 / pk["hbm_gbs"],
+                             "algorithmic_bytes": alg_bytes, "visible_pairs": vis,
+                             "visible_pair_tflops": vis * 2.0 * wl.H * wl.D / ms / 1e9,
+                             "launches": 2, "l2": "256 MB flush before each call"}
+        tidx = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.int32, device="cuda")
+        tsc = torch.empty(wl.B, wl.S, wl.topk, dtype=torch.bfloat16, device="cuda")
+        wsb = lidx.lidx_workspace_bytes(lidx.OP_TOPK_V41, wl.B, wl.S, wl.Skv, wl.H, wl.D, wl.topk, True)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+        fn = lambda: lidx.lidx_indexer_topk_v41(q, k, w, allowed, wl.topk, out=(out16, tidx, tsc),
+                                                workspace=ws)
+        for _ in range(3):
+            fn()
+        ms2 = _median_ms(fn, stream, 10, flush)
+        out["v41_packed_topk"] = {"ms": ms2, "topk": wl.topk, "selection_ms": ms2 - ms,
+                                  "rows_per_s": wl.B * wl.S / ms2 * 1e3, "launches": 3,
+                                  "l2": "256 MB flush before each call"}
+        del q, k, w, allowed, out16, ws, tidx, tsc
+
+    def _selection():
+        # selection alone on adversarial rows: time of a tie-heavy row against a normal one
+        rows, Skv, topk = 4096, 4096, 2048
+        sel = {}
+        for kind in ("normal", "ties", "const", "zero_pad", "two_values"):
+            x = selection_rows(kind, rows, Skv).cuda()
+            oi = torch.empty(rows, topk, dtype=torch.int32, device="cuda")
+            os_ = torch.empty(rows, topk, dtype=torch.float32, device="cuda")
+            fn = lambda: lidx.lidx_topk_rows(x, topk, out=(oi, os_))
+            for _ in range(3):
+                fn()
+            sel[kind] = time_steps(fn, 10, stream)
+            del x, oi, os_
+        out["selection"] = {"rows": rows, "Skv": Skv, "topk": topk, "ms": sel,
+                            "worst_over_normal": max(sel.values()) / sel["normal"],
+                            "kernel": "topk_rows_kernel (standalone selection, 256 threads per row)"}
+
+    def _bwd():
+        # backward through the selected entries (selection: the forward's own top-k)
+        wl = workloads.WORKLOADS["bwd"]
+        q, k, w = [t.cuda() for t in workloads.v4_inputs(wl, 0)]
+        idx, _, _ = lidx.lidx_indexer_fwd(q, k, w, wl.ratio, wl.topk)
+        grad = workloads.grad_scores(wl.B, wl.S, wl.topk, 0).cuda()
+        outs = (torch.empty(wl.S, wl.B, wl.H, wl.D, device="cuda"), torch.empty(wl.Skv, wl.B, wl.D, device="cuda"),
+                torch.empty(wl.S, wl.B, wl.H, device="cuda"))
+        wsb = lidx.lidx_workspace_bytes(lidx.OP_INDEXER_BWD, wl.B, wl.S, wl.Skv, wl.H, wl.D, wl.topk)
+        ws = torch.empty(max(wsb, 1), dtype=torch.uint8, device="cuda")
+        fn = lambda: lidx.lidx_indexer_bwd(q, k, w, idx, grad, wl.ratio, out=outs, workspace=ws)
+        for _ in range(2):
+            fn()
+        ms = time_steps(fn, 10, stream)
+        nsel = int((idx >= 0).sum().item())
+        fl = nsel * 6.0 * wl.H * wl.D
+        out["bwd"] = {"ms": ms, "selected_pairs": nsel, "tflops": fl / ms / 1e9,
+                      "tensor_frac": fl / ms / 1e9 / pk["bf16_tflops"], "kernel": BWD_KERNEL,
+                      "launches": 4, "algorithmic": "6*H*D FLOP per selected pair",
+                      "workspace_bytes": wsb}
+        del q, k, w, idx, grad, outs, ws
+
+    for name, f in (("tiny", _tiny), ("c4_fwd", _c4_fwd), ("v41_packed", _v41_packed),
+                    ("selection", _selection), ("bwd", _bwd)):
+        if names is None or name in names:
+            f()
     return out
-
 
 BWD_KERNEL = ("bwd_scatter_kernel + bwd_tile_kernel<64,0> (dq, dw) + bwd_tile_kernel<64,1> (dk partials) "
               "+ bwd_reduce_kernel; tcgen05, P as bf16 hi+lo from TMEM")
@@ -556,7 +566,7 @@ def emit(args, wl, world, ms, ms_max, flops, pairs, value, rows_per_s, e2e_ms, h
         "device_status": status,
     }
     if not args.no_side:
-        line["other_workloads"] = side_workloads(lidx, pk)
+        line["other_workloads"] = side_workloads(lidx, pk, args.side.split(",") if args.side else None)
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_oracle_sample(wl, args.cpu_stride)
     print(json.dumps(line), flush=True)
@@ -577,6 +587,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-side", action="store_true")
+    ap.add_argument("--side", default="", help="comma-separated subset of the side measurements "
+                    "(tiny, c4_fwd, v41_packed, selection, bwd); default all")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
