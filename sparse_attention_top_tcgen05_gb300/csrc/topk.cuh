@@ -35,6 +35,9 @@
 //      over the exact value range of its members, bucketed by key; a few such
 //      refinements end in buckets that fit or in all-equal items.  Histogram
 //      and scatter combine the atomics of runs of one bucket (ties).
+// A row of at most kTopkShort keys skips all this: one warp turns each entry
+// into a 64-bit key (order key of the score, then the complement of its
+// offset) and sorts the keys in registers.
 #pragma once
 #include <limits.h>
 #include <stdint.h>
