@@ -158,7 +158,6 @@ __device__ __forceinline__ uint32_t v41_weight_word(const ScoreParams& p, int u,
     return (uint32_t)wr[0];
 }
 
-__device__ __forceinline__ float act_f(float x, int act) { return act == 0 ? fmaxf(x, 0.f) : x; }
 
 struct SmemLayout {
     uint32_t q_off, k_off, w_off, range_off, topk_off, bar_off, tmem_off, total;
@@ -185,55 +184,37 @@ __host__ __device__ inline SmemLayout smem_layout(int D) {
     return L;
 }
 
-// Weighted head reduction of one query's H accumulator columns held in
-// registers r[c0 .. c0+H) (c0 compile time): sum_h w[h] * act(x[h]).
-// Weighted head sum of HH consecutive columns starting at c0 of a 32-column
-// chunk held in registers (c0 is a constant once the caller's loops unroll).
-template <int HH>
-__device__ __forceinline__ float head_sum_at(const uint32_t (&r)[32], int c0, const float* w, int act) {
+// (a0, a1) += (w0 * x0, w1 * x1): two fp32 fused multiply-adds in one packed
+// instruction, each rounded as fmaf rounds it.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float w0, float w1, float x0, float x1) {
+    asm("{\n\t.reg .b64 x, w, s;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 w, {%4, %5};\n\t"
+        "mov.b64 s, {%0, %1};\n\tfma.rn.f32x2 s, w, x, s;\n\tmov.b64 {%0, %1}, s;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(x0), "f"(x1), "f"(w0), "f"(w1));
+}
+
+// Weighted head sum sum_h w[h] * act(x[h]) of HH consecutive accumulator
+// columns starting at c0 of a 32-column chunk held in registers (c0 is a
+// constant once the caller's loops unroll); act is ReLU when RELU.  Four
+// independent fp32 chains, two per packed instruction, weights from shared
+// memory four at a time.
+template <int HH, bool RELU>
+__device__ __forceinline__ float head_sum_at(const uint32_t (&r)[32], int c0, const float* w) {
+    auto act = [](float x) { return RELU ? fmaxf(x, 0.f) : x; };
     if constexpr (HH >= 4) {
         const float4* w4 = reinterpret_cast<const float4*>(w);
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int h = 0; h < HH; h += 4) {
             const float4 wv = w4[h / 4];
-            a0 = fmaf(wv.x, act_f(__uint_as_float(r[c0 + h]), act), a0);
-            a1 = fmaf(wv.y, act_f(__uint_as_float(r[c0 + h + 1]), act), a1);
-            a2 = fmaf(wv.z, act_f(__uint_as_float(r[c0 + h + 2]), act), a2);
-            a3 = fmaf(wv.w, act_f(__uint_as_float(r[c0 + h + 3]), act), a3);
+            fma2(a0, a1, wv.x, wv.y, act(__uint_as_float(r[c0 + h])), act(__uint_as_float(r[c0 + h + 1])));
+            fma2(a2, a3, wv.z, wv.w, act(__uint_as_float(r[c0 + h + 2])), act(__uint_as_float(r[c0 + h + 3])));
         }
         return (a0 + a1) + (a2 + a3);
     } else {
         float acc = 0.f;
 #pragma unroll
-        for (int h = 0; h < HH; ++h) acc = fmaf(w[h], act_f(__uint_as_float(r[c0 + h]), act), acc);
-        return acc;
-    }
-}
-
-template <int H, int C0, int NR>
-__device__ __forceinline__ float head_sum(const uint32_t (&r)[NR], const float* w, int act) {
-    if constexpr (H >= 4) {
-        // four independent FMA chains; weights come four at a time from shared memory
-        const float4* w4 = reinterpret_cast<const float4*>(w);
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-        for (int h = 0; h < H; h += 4) {
-            const float4 wv = w4[h / 4];
-            const float x0 = act_f(__uint_as_float(r[C0 + h]), act);
-            const float x1 = act_f(__uint_as_float(r[C0 + h + 1]), act);
-            const float x2 = act_f(__uint_as_float(r[C0 + h + 2]), act);
-            const float x3 = act_f(__uint_as_float(r[C0 + h + 3]), act);
-            a0 = fmaf(wv.x, x0, a0);
-            a1 = fmaf(wv.y, x1, a1);
-            a2 = fmaf(wv.z, x2, a2);
-            a3 = fmaf(wv.w, x3, a3);
-        }
-        return (a0 + a1) + (a2 + a3);
-    } else {
-        float acc = 0.f;
-#pragma unroll
-        for (int h = 0; h < H; ++h) acc = fmaf(w[h], act_f(__uint_as_float(r[C0 + h]), act), acc);
+        for (int h = 0; h < HH; ++h) acc = fmaf(w[h], act(__uint_as_float(r[c0 + h])), acc);
         return acc;
     }
 }
@@ -709,7 +690,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (lane == 0) mbar_arrive(acc_empty + acc);  // accumulator may be reused
                     }
                     if constexpr (H >= 32) {
-                        run += head_sum_at<32>(r, 0, wh + c * 32, p.act);
+                        run += relu ? head_sum_at<32, true>(r, 0, wh + c * 32)
+                                    : head_sum_at<32, false>(r, 0, wh + c * 32);
                         if (((c + 1) * 32) % H == 0) {
                             store(half * QH + (c * 32) / H, run);
                             run = 0.f;
@@ -718,7 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int qq = 0; qq < 32 / H; ++qq)
                             store(half * QH + c * (32 / H) + qq,
-                                  head_sum_at<H>(r, qq * H, wh + c * 32 + qq * H, p.act));
+                                  relu ? head_sum_at<H, true>(r, qq * H, wh + c * 32 + qq * H)
+                                       : head_sum_at<H, false>(r, qq * H, wh + c * 32 + qq * H));
                     }
                 }
             }
