@@ -305,8 +305,8 @@ size_t lidx_workspace_bytes(int op, int64_t B, int64_t S, int64_t Skv, int H, in
         // one byte per (batch, query tile, 128-key tile): the visibility tile map
         if (Skv <= 0) return 0;
         const int64_t QT = score_query_tile(H), units = B * ((S + QT - 1) / QT);
-        // the tile map, then each query tile's record (key-tile range and tile mask)
-        const int64_t map = (units * ((Skv + 127) / 128) + 255) / 256 * 256 + (units * 16 + 255) / 256 * 256;
+        // the tile map: one byte per (batch, query tile, 128-key tile)
+        const int64_t map = (units * ((Skv + 127) / 128) + 255) / 256 * 256;
         if (op == LIDX_OP_SCORES_V41 || logits_materialised) return (size_t)map;
         return (size_t)(map + (B * S * Skv * 2 + 255) / 256 * 256);  // + the bf16 scores
     }
@@ -419,12 +419,8 @@ int lidx_topk_rows(const float* logits, int64_t rows, int64_t S, int64_t Skv, in
 static int scores_v41_impl(const void* q, const void* k, const void* w, const uint8_t* allowed,
                            int64_t B, int64_t S, int64_t Skv, int H, int D, int act,
                            void* scores_out, uint8_t* tilemap, int sms, cudaStream_t st) {
-    const int64_t QT = score_query_tile(H), units = B * ((S + QT - 1) / QT);
-    int4* urec = (int4*)(tilemap + (units * ((Skv + 127) / 128) + 255) / 256 * 256);
-    // 1. visibility pass: tile map and each query tile's record
-    if (v41_mask_launch(allowed, tilemap, urec, (int)B, (int)S, (int)Skv, (int)QT, st) != cudaSuccess)
-        return LIDX_ERR_CUDA;
-    // 2. tensor-core pass over the blocks with a visible pair; -inf over the rest
+    // one launch: visibility of each (query tile, key tile) block, the tensor-core
+    // pass over the blocks with a visible pair, -inf over the rest
     ScoreLaunch a;
     memset(&a, 0, sizeof a);
     a.p.B = (int)B;
@@ -438,7 +434,6 @@ static int scores_v41_impl(const void* q, const void* k, const void* w, const ui
     a.p.allowed = allowed;
     a.p.out16 = (uint16_t*)scores_out;
     a.p.tilemap = tilemap;
-    a.p.urec = urec;
     a.q = q;
     a.k = k;
     a.stream = st;

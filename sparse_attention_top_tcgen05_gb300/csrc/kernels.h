@@ -25,9 +25,7 @@ struct ScoreParams {
     const uint16_t* w16;      // [B,S,H] bf16
     const uint8_t* allowed;   // [B,S,Skv]
     uint16_t* out16;          // [B,S,Skv] bf16
-    const uint8_t* tilemap;   // [B, qtiles, ntk]: 1 where the block has a visible pair
-    const int4* urec;         // [B, qtiles]: {x, y, m0, m1}: key tiles [x, y) hold the query tile's
-                              // visible pairs; bit j of (m1:m0) = block of key tile x + j has one
+    uint8_t* tilemap;         // [B, qtiles, ntk]: 1 where the block has a visible pair (written by the kernel)
     int ntk;                  // key tiles per row
     int vis_tma;              // 1: visibility flags staged by TMA (set by the launcher)
     const int32_t* idx_in;    // nullable [B,S,topk]: score these keys instead of selecting
@@ -54,8 +52,6 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* ad
 int score_fwd_launch(ScoreLaunch& a);
 int score_v41_launch(ScoreLaunch& a);
 int score_query_tile(int H);  // query rows per tile for H heads
-cudaError_t v41_mask_launch(const uint8_t* allowed, uint8_t* tilemap, int4* urec, int B, int S, int Skv,
-                            int QT, cudaStream_t stream);
 size_t score_scratch_bytes(int64_t S, int64_t Skv, int H, int num_sms);
 
 cudaError_t extract_launch(const float* logits, const int32_t* idx, int64_t rows, int64_t Skv,

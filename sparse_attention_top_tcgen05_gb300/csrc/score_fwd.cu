@@ -48,6 +48,9 @@ constexpr int kTopkBar = 2;        // named barrier ids of the selection groups:
 constexpr int kTopkGroups = 3;     // rows selected concurrently
 constexpr int kTopkGroupThreads = kTopkThreads / kTopkGroups;
 constexpr int kVisStages = 4;      // V4.1: ring of staged visibility blocks
+constexpr int kRecSlots = 4;       // V4.1: ring of per-unit visibility records
+constexpr int kFillBar = 5;        // V4.1: named barrier id of the visibility / fill warps
+constexpr int kRecBitTiles = 512;  // V4.1: key tiles whose activity a record's builder keeps in bits
 
 struct Unit {
     int b, s0, qt;
@@ -78,7 +81,7 @@ __device__ __forceinline__ Unit make_unit(const ScoreParams& p, int u, const int
     un.s0 = qt * QT;
     const int s_last = min(un.s0 + QT - 1, p.S - 1);
     if constexpr (V41) {
-        // the range of key tiles with visible pairs comes from the visibility pass
+        // the range of key tiles with visible pairs comes from the unit's record
         un.lo_t = rec.x;
         un.hi_t = rec.y;
         un.bits = (uint64_t)(uint32_t)rec.z | ((uint64_t)(uint32_t)rec.w << 32);
@@ -132,18 +135,6 @@ __device__ __forceinline__ int unit_of(int i, int num_units) {
     return u < num_units ? u : -1;
 }
 
-// V4.1: the visibility record of this CTA's i-th unit (zeros where there is
-// none).  Each role loads the next unit's record one step ahead, so that the
-// load's latency overlaps the current unit.
-template <bool V41>
-__device__ __forceinline__ int4 unit_rec(const ScoreParams& p, int i) {
-    if constexpr (V41) {
-        const int u = unit_of(i, p.num_units);
-        if (u >= 0) return p.urec[(size_t)(u % p.B) * p.qtiles + (p.qtiles - 1 - u / p.B)];
-    }
-    return make_int4(0, 0, 0, 0);
-}
-
 // V4.1: word e of a unit's bf16 weights, laid out as the epilogue keeps them:
 // heads (2e, 2e+1) of query 2e / H in one word (one weight per word at H = 1);
 // zero past the sequence, for threads past the tile's words and for u < 0.
@@ -177,7 +168,7 @@ __host__ __device__ inline SmemLayout smem_layout(int D) {
     L.topk_off = o;
     o += (uint32_t)(kTopkGroups * ((sizeof(TopkSmem) + 15) / 16 * 16));
     L.bar_off = o;
-    o += 24 * 8;
+    o += 32 * 8;
     L.tmem_off = o;
     o += 16;
     L.total = o + 1024;  // slack for 1024-byte alignment of the base
@@ -304,6 +295,14 @@ __device__ __forceinline__ void row_gather(const float* row, int lo, int hi, con
     named_bar_sync(bar_id, NT);
 }
 
+// V4.1: what the visibility warps gather about one unit before its record is
+// written: the first and last key tile with a visible pair, and one bit per key
+// tile for the first kRecBitTiles tiles.
+struct RecBuild {
+    int first, last;
+    uint32_t bits[kRecBitTiles / 32];
+};
+
 template <int H, bool V41>
 __global__ void __launch_bounds__(kThreads, 1)
     score_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -333,16 +332,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // V4.1 (QT <= 32): the visibility flags of each computed block, QT rows of
     // 128 bytes, come by TMA into a ring after the second query tile
     constexpr bool VIS_RING = V41 && QT <= 32;
-    // then each epilogue warp's own copy of its weights (up to 64 words a warp)
+    // then each epilogue warp's own copy of its weights (up to 64 words a warp),
+    // the record ring, the record builder's state (two) and an abort flag
     static_assert(kTopkGroups * ((sizeof(TopkSmem) + 15) / 16 * 16) >=
-                      (size_t)kN * 128 * 2 + kVisStages * 32 * kM + 16 * 64 * 4,
-                  "second query tile, visibility ring and weights exceed the scratch");
+                      (size_t)kN * 128 * 2 + kVisStages * 32 * kM + 16 * 64 * 4 + kRecSlots * 16 +
+                          2 * sizeof(RecBuild) + 16,
+                  "second query tile, visibility ring, weights and records exceed the scratch");
     const bool vis_tma = VIS_RING && p.vis_tma;
     uint8_t* const sQ1 = smem + L.topk_off;  // second query tile (V4.1 only)
     uint8_t* const sVis = sQ1 + kN * p.D * 2;
     uint32_t* const sWw = reinterpret_cast<uint32_t*>(sVis + kVisStages * 32 * kM);  // [EW][64]
+    int4* const sRec = reinterpret_cast<int4*>(sWw + 16 * 64);                        // [kRecSlots]
+    RecBuild* const sBuild = reinterpret_cast<RecBuild*>(sRec + kRecSlots);           // [2]
+    int* const sAbort = reinterpret_cast<int*>(sBuild + 2);
     uint64_t* vis_full = bars + 16;   // [kVisStages]
     uint64_t* vis_empty = bars + 20;  // [kVisStages]
+    uint64_t* rec_full = bars + 24;   // [kRecSlots] record c written
+    uint64_t* rec_empty = bars + 28;  // [kRecSlots] record c read by every other role
     auto sQb = [&](int qb) { return qb ? sQ1 : sQ; };
     auto q_fullv = [&](int qb) { return bars + (qb ? 14 : 0); };
     auto q_emptyv = [&](int qb) { return bars + (qb ? 15 : 1); };
@@ -379,6 +385,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(vis_full + i, 1);
                 mbar_init(vis_empty + i, EW);
             }
+        if (V41)
+            for (int i = 0; i < kRecSlots; ++i) {
+                mbar_init(rec_full + i, 1);
+                mbar_init(rec_empty + i, 2 + EW);  // producer, MMA issuer, each epilogue warp
+            }
         fence_mbar_init();
         tma_prefetch_desc(&tmq);
         tma_prefetch_desc(&tmk);
@@ -392,22 +403,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    // V4.1: the visibility records come from the preceding pass, which may still
-    // be finishing when this grid starts (programmatic launch)
-    if constexpr (V41) griddep_wait();
+    // V4.1: record c of the CTA's sequence of units, copied out of its ring slot,
+    // which is then released (one arrival per role, per epilogue warp)
+    auto rec_take = [&](int c, int4& rec) -> bool {
+        if (!mbar_wait(rec_full + c % kRecSlots, (c / kRecSlots) & 1, p.wait_ns)) return false;
+        rec = sRec[c % kRecSlots];
+        return true;
+    };
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && !p.debug_stall) {
             int kcount = 0, qcount = 0;
             bool ok = true;
-            int4 rec_next = unit_rec<V41>(p, 0);
+            int c = 0;  // units taken so far (V4.1 record index)
             for (int i = 0; ok; ++i) {
                 const int u = unit_of(i, p.num_units);
                 if (u == -2) break;
-                const int4 rec = rec_next;
-                rec_next = unit_rec<V41>(p, i + 1);
                 if (u < 0) continue;
+                int4 rec = make_int4(0, 0, 0, 0);
+                if constexpr (V41) {
+                    if (!(ok = rec_take(c, rec))) break;
+                    mbar_arrive(rec_empty + c % kRecSlots);
+                    ++c;
+                }
                 const Unit un = make_unit<QT, V41>(p, u, rec);
                 if (un.hi_t <= un.lo_t) continue;
                 const int qb = qcount % NQB;
@@ -475,13 +494,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             int kcount = 0, tcount = 0, qcount = 0;
             bool ok = true;
-            int4 rec_next = unit_rec<V41>(p, 0);
+            int c = 0;  // units taken so far (V4.1 record index)
             for (int i = 0; ok; ++i) {
                 const int u = unit_of(i, p.num_units);
                 if (u == -2) break;
-                const int4 rec = rec_next;
-                rec_next = unit_rec<V41>(p, i + 1);
                 if (u < 0) continue;
+                int4 rec = make_int4(0, 0, 0, 0);
+                if constexpr (V41) {
+                    if (!(ok = rec_take(c, rec))) break;
+                    mbar_arrive(rec_empty + c % kRecSlots);
+                    ++c;
+                }
                 const Unit un = make_unit<QT, V41>(p, u, rec);
                 if (un.hi_t <= un.lo_t) continue;
                 const int qb = qcount % NQB;
@@ -527,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ntiles_all = (p.Skv + kM - 1) / kM;
         int tcount = 0, ucount = 0;
         bool ok = true;
-        int4 rec_next = unit_rec<V41>(p, 0);
+        int c = 0;  // units taken so far (V4.1 record index)
         // V4.1: accumulator columns of this warp (64 or 128), its whole queries, and
         // its weight words per lane, held one unit ahead
         constexpr int CPW = 4 * kN / EW, QW = CPW / H, WPER = H >= 2 ? 2 : 1;
@@ -541,9 +564,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; ok; ++i) {
             const int u = unit_of(i, p.num_units);
             if (u == -2) break;
-            const int4 rec = rec_next;
-            rec_next = unit_rec<V41>(p, i + 1);
             if (u < 0) continue;
+            int4 rec = make_int4(0, 0, 0, 0);
+            if constexpr (V41) {
+                if (!(ok = rec_take(c, rec))) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rec_empty + c % kRecSlots);
+                ++c;
+            }
             const Unit un = make_unit<QT, V41>(p, u, rec);
             if constexpr (V41) {
                 const int q0 = half * QW;  // this warp's first query within the tile
@@ -559,7 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 __syncwarp();
                 for (int kt = un.lo_t; kt < un.hi_t; ++kt) {
-                    if (!tile_active<V41>(p, un, kt)) continue;  // written as -inf by the mask pass
+                    if (!tile_active<V41>(p, un, kt)) continue;  // written as -inf by the fill warps
                     const int t = kt * kM + row_t;
                     const int acc = tcount & 1, vs = tcount % kVisStages;
                     const uint32_t vph = (tcount / kVisStages) & 1;
@@ -713,22 +741,169 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++ucount;
         }
     } else if constexpr (V41) {
-        // ---------------------------------------------------------- -inf fill
-        // The remaining warps write -inf over every block of the CTA's units that
-        // holds no visible pair, while the tensor-core sweep computes the others:
-        // each output element is written once, by this fill or by the epilogue.
-        constexpr int FT = kThreads - 64 - EWT;
-        const int ftid = threadIdx.x - 64 - EWT;
+        // ------------------------------------------------- visibility and fill
+        // The remaining warps read each unit's rows of `allowed` once, publish the
+        // unit's record (its range of key tiles with a visible pair and their
+        // activity bits) one unit ahead of its use, and write -inf over every block
+        // of the unit that holds no visible pair, while the tensor-core sweep
+        // computes the others: each output element is written once, by this fill
+        // or by the epilogue.
+        constexpr int FT = kThreads - 64 - EWT, FW = FT / 32;
+        const int ftid = threadIdx.x - 64 - EWT, fw = ftid >> 5;
         const bool vec = (p.Skv % 8) == 0 && (((uintptr_t)p.out16) & 15) == 0;
+        const bool vec16 = (p.Skv % 16) == 0 && (((uintptr_t)p.allowed) & 15) == 0;
+        const bool vec4 = (p.Skv % 4) == 0 && (((uintptr_t)p.allowed) & 3) == 0;
         const uint4 ninf4 = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
-        int4 rec_next = unit_rec<true>(p, 0);
-        for (int i = 0;; ++i) {
-            const int u = unit_of(i, p.num_units);
-            if (u == -2) break;
-            const int4 rec = rec_next;
-            rec_next = unit_rec<true>(p, i + 1);
-            if (u < 0) continue;
-            const Unit un = make_unit<QT, true>(p, u, rec);
+        const int ntk = p.ntk;
+        // Record c (unit u): key-tile flags into the tile map and the builder's
+        // state, then warp 0 of this role writes the ring slot.  False when the
+        // slot did not come free in time.
+        auto build_record = [&](int c, int u) -> bool {
+            RecBuild& st = sBuild[c & 1];  // the other one may still be read by warp 0
+            const int slot = c % kRecSlots;
+            if (ftid == 0)
+                *sAbort = mbar_wait(rec_empty + slot, ((c / kRecSlots) & 1) ^ 1, p.wait_ns) ? 0 : 1;
+            if (ftid == 0) st.first = ntk;
+            if (ftid == 1) st.last = -1;
+            if (ftid >= 2 && ftid < 2 + kRecBitTiles / 32) st.bits[ftid - 2] = 0u;
+            named_bar_sync(kFillBar, FT);
+            if (*sAbort) return false;
+            const int b = u % p.B, qt = p.qtiles - 1 - u / p.B, s0 = qt * QT;
+            const int rows = min(QT, p.S - s0);
+            uint8_t* const map = p.tilemap + ((size_t)b * p.qtiles + qt) * ntk;
+            const uint8_t* const ubase = p.allowed + ((size_t)b * p.S + s0) * p.Skv;
+            auto mark = [&](int kt, bool active) {
+                map[kt] = active ? 1 : 0;
+                if (active) {
+                    atomicMin(&st.first, kt);
+                    atomicMax(&st.last, kt);
+                    if (kt < kRecBitTiles) atomicOr(&st.bits[kt >> 5], 1u << (kt & 31));
+                }
+            };
+            if (vec16) {
+                // a lane reads 16 flags of a row; 8 lanes cover a key tile, a warp 512 keys
+                // two chunks of a warp in flight together
+                const int nch = (ntk + 3) / 4;
+                for (int ch0 = fw; ch0 < nch; ch0 += 2 * FW) {
+                    uint32_t acc[2] = {0u, 0u};
+                    bool in[2];
+                    const uint8_t* base[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int t0 = (ch0 + h * FW) * 512 + lane * 16;
+                        in[h] = t0 < p.Skv;  // Skv % 16 == 0: all 16 keys inside or none
+                        base[h] = ubase + (in[h] ? t0 : 0);
+                    }
+                    int r = 0;
+                    for (; r + 4 <= rows; r += 4) {
+                        uint4 v[2][4];
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q)
+                                v[h][q] = in[h] ? *reinterpret_cast<const uint4*>(base[h] + (size_t)(r + q) * p.Skv)
+                                                : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) acc[h] |= v[h][q].x | v[h][q].y | v[h][q].z | v[h][q].w;
+                    }
+                    for (; r < rows; ++r)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint4 v = in[h] ? *reinterpret_cast<const uint4*>(base[h] + (size_t)r * p.Skv)
+                                                  : make_uint4(0u, 0u, 0u, 0u);
+                            acc[h] |= v.x | v.y | v.z | v.w;
+                        }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t any = acc[h] != 0 ? 1u : 0u;
+                        any |= __shfl_xor_sync(0xffffffffu, any, 1);
+                        any |= __shfl_xor_sync(0xffffffffu, any, 2);
+                        any |= __shfl_xor_sync(0xffffffffu, any, 4);
+                        const int kt = (ch0 + h * FW) * 4 + (lane >> 3);
+                        if ((lane & 7) == 0 && kt < ntk) mark(kt, any != 0);
+                    }
+                }
+            } else {
+                // a lane reads 4 flags of a row (one word when rows are 4-byte aligned)
+                for (int kt = fw; kt < ntk; kt += FW) {
+                    const int t0 = kt * kM + lane * 4;
+                    uint32_t any = 0;
+                    for (int r = 0; r < rows; ++r) {
+                        const uint8_t* row = ubase + (size_t)r * p.Skv;
+                        if (vec4 && t0 + 3 < p.Skv) {
+                            any |= *reinterpret_cast<const uint32_t*>(row + t0);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j)
+                                if (t0 + j < p.Skv) any |= row[t0 + j];
+                        }
+                    }
+                    const bool active = __any_sync(0xffffffffu, any != 0);
+                    if (lane == 0) mark(kt, active);
+                }
+            }
+            named_bar_sync(kFillBar, FT);  // the unit's flags are all in
+            if (fw == 0) {
+                const int first = st.first, last = st.last;
+                int4 r = make_int4(0, 0, 0, 0);
+                if (last >= 0) {
+                    auto active = [&](int kt) {
+                        if (kt > last) return false;
+                        if (kt < kRecBitTiles) return ((st.bits[kt >> 5] >> (kt & 31)) & 1u) != 0u;
+                        return map[kt] != 0;
+                    };
+                    const uint32_t m0 = __ballot_sync(0xffffffffu, active(first + lane));
+                    const uint32_t m1 = __ballot_sync(0xffffffffu, active(first + 32 + lane));
+                    r = make_int4(first, last + 1, (int)m0, (int)m1);
+                }
+                if (lane == 0) {
+                    sRec[slot] = r;
+                    mbar_arrive(rec_full + slot);  // release: the record and the tile map row
+                }
+            }
+            return true;
+        };
+        // the CTA's next unit from position i on (-2 past the end)
+        auto next_unit = [&](int& i) {
+            int u;
+            do {
+                u = unit_of(i++, p.num_units);
+            } while (u == -1);
+            return u;
+        };
+        // the rows of unit u into L2 ahead of its record (16-byte aligned rows only)
+        auto prefetch_rows = [&](int u) {
+            if (u < 0 || !vec16 || ftid != 0) return;
+            const int b = u % p.B, s0 = (p.qtiles - 1 - u / p.B) * QT;
+            const uint8_t* src = p.allowed + ((size_t)b * p.S + s0) * p.Skv;
+            size_t left = (size_t)min(QT, p.S - s0) * p.Skv;  // contiguous rows
+            for (; left > 0; src += 16384) {
+                const uint32_t n = left < 16384 ? (uint32_t)left : 16384u;
+                bulk_prefetch_l2(src, n);
+                left -= n;
+            }
+        };
+        int i = 0, c = 0;
+        int u = next_unit(i);
+        {
+            int ip = i;
+            prefetch_rows(next_unit(ip));
+        }
+        bool ok = u < 0 || build_record(0, u);
+        while (ok && u >= 0) {
+            const int u_next = next_unit(i);
+            {
+                int ip = i;
+                prefetch_rows(next_unit(ip));  // the unit after next
+            }
+            if (u_next >= 0)
+                ok = build_record(c + 1, u_next);  // one unit ahead of its use
+            else
+                named_bar_sync(kFillBar, FT);  // record c is visible to the whole role
+            if (!ok) break;
+            const Unit un = make_unit<QT, true>(p, u, sRec[c % kRecSlots]);
             const int rows = min(QT, p.S - un.s0);
             // keys [a, b) of every row of the unit; a and b multiples of 8 when vec
             auto fill = [&](int a, int b) {
@@ -750,6 +925,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 fill(0, p.Skv);
             }
+            u = u_next;
+            ++c;
         }
     } else {
         // ------------------------------------------------------------ top-k
@@ -843,24 +1020,8 @@ static cudaError_t launch_h(const ScoreLaunch& a, const CUtensorMap& mq, const C
     auto kern = score_fwd_kernel<H, V41>;
     cudaError_t e = set_smem_attr((const void*)kern, smem);
     if (e != cudaSuccess) return e;
-    if constexpr (!V41) {
-        kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, ma, a.p);
-        return cudaGetLastError();
-    }
-    // V4.1 follows its visibility pass on the stream: launched so that its
-    // set-up overlaps the end of that pass (it waits for the records itself)
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cfg.stream = (cudaStream_t)a.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, mq, mk, ma, a.p);
+    kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, ma, a.p);
+    return cudaGetLastError();
 }
 
 template <bool V41>
@@ -913,8 +1074,9 @@ int score_fwd_launch(ScoreLaunch& a) {
     return e == cudaSuccess ? 0 : -1;
 }
 
-// V4.1: q [B,S,H,D], k [B,Skv,D].  Key tiles come from p.tilemap, built by the
-// mask pass, which also wrote -inf for every block it marked empty.
+// V4.1: q [B,S,H,D], k [B,Skv,D], allowed [B,S,Skv].  One launch: the kernel's
+// visibility warps read `allowed` and build each unit's record and tile map row
+// (p.tilemap, caller workspace) ahead of the tensor-core sweep.
 int score_v41_launch(ScoreLaunch& a) {
     ScoreParams& p = a.p;
     p.wait_ns = wait_limit_ns();
