@@ -307,8 +307,10 @@ size_t lidx_workspace_bytes(int op, int64_t B, int64_t S, int64_t Skv, int H, in
         const int64_t QT = score_query_tile(H), units = B * ((S + QT - 1) / QT);
         // the tile map: one byte per (batch, query tile, 128-key tile)
         const int64_t map = (units * ((Skv + 127) / 128) + 255) / 256 * 256;
-        if (op == LIDX_OP_SCORES_V41 || logits_materialised) return (size_t)map;
-        return (size_t)(map + (B * S * Skv * 2 + 255) / 256 * 256);  // + the bf16 scores
+        if (op == LIDX_OP_SCORES_V41) return (size_t)map;
+        const int64_t ranges = (units * 8 + 255) / 256 * 256;  // each query tile's key-tile range
+        if (logits_materialised) return (size_t)(map + ranges);
+        return (size_t)(map + ranges + (B * S * Skv * 2 + 255) / 256 * 256);  // + the bf16 scores
     }
     if (op == LIDX_OP_INDEXER_BWD) return bwd_workspace_bytes(B, S, Skv, H, D, topk, sms);
     return 0;
@@ -418,7 +420,7 @@ int lidx_topk_rows(const float* logits, int64_t rows, int64_t S, int64_t Skv, in
 // V4.1 scoring into `scores_out` (bf16 [B,S,Skv]); the tile map goes to `tilemap`.
 static int scores_v41_impl(const void* q, const void* k, const void* w, const uint8_t* allowed,
                            int64_t B, int64_t S, int64_t Skv, int H, int D, int act,
-                           void* scores_out, uint8_t* tilemap, int sms, cudaStream_t st) {
+                           void* scores_out, uint8_t* tilemap, int2* urange, int sms, cudaStream_t st) {
     // one launch: visibility of each (query tile, key tile) block, the tensor-core
     // pass over the blocks with a visible pair, -inf over the rest
     ScoreLaunch a;
@@ -434,6 +436,7 @@ static int scores_v41_impl(const void* q, const void* k, const void* w, const ui
     a.p.allowed = allowed;
     a.p.out16 = (uint16_t*)scores_out;
     a.p.tilemap = tilemap;
+    a.p.urange = urange;
     a.q = q;
     a.k = k;
     a.stream = st;
@@ -456,7 +459,7 @@ int lidx_indexer_scores_v41(const void* q, const void* k, const void* w, const u
     if (sms <= 0) return LIDX_ERR_NO_DEVICE;
     const size_t need = lidx_workspace_bytes(LIDX_OP_SCORES_V41, B, S, Skv, H, D, 0, 0);
     if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u)) return LIDX_ERR_WORKSPACE;
-    return scores_v41_impl(q, k, w, allowed, B, S, Skv, H, D, act, scores_out, (uint8_t*)workspace,
+    return scores_v41_impl(q, k, w, allowed, B, S, Skv, H, D, act, scores_out, (uint8_t*)workspace, nullptr,
                            sms, (cudaStream_t)stream);
 }
 
@@ -486,11 +489,17 @@ int lidx_indexer_topk_v41(const void* q, const void* k, const void* w, const uin
         lidx_workspace_bytes(LIDX_OP_TOPK_V41, B, S, Skv, H, D, topk, scores_out != nullptr);
     if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255u))
         return LIDX_ERR_WORKSPACE;
+    // workspace: tile map, then each query tile's key-tile range, then (unless kept
+    // by the caller) the bf16 scores
     const size_t map_bytes = lidx_workspace_bytes(LIDX_OP_SCORES_V41, B, S, Skv, H, D, 0, 0);
-    uint16_t* scores = scores_out ? (uint16_t*)scores_out : (uint16_t*)((uint8_t*)workspace + map_bytes);
-    rc = scores_v41_impl(q, k, w, allowed, B, S, Skv, H, D, act, scores, (uint8_t*)workspace, sms, st);
+    const int64_t QT = score_query_tile(H), units = B * ((S + QT - 1) / QT);
+    int2* urange = (int2*)((uint8_t*)workspace + map_bytes);
+    const size_t range_bytes = (size_t)(units * 8 + 255) / 256 * 256;
+    uint16_t* scores =
+        scores_out ? (uint16_t*)scores_out : (uint16_t*)((uint8_t*)workspace + map_bytes + range_bytes);
+    rc = scores_v41_impl(q, k, w, allowed, B, S, Skv, H, D, act, scores, (uint8_t*)workspace, urange, sms, st);
     if (rc) return rc;
-    return topk_rows_bf16_launch(scores, rows, (int)Skv, topk, indices_out,
+    return topk_rows_bf16_launch(scores, rows, (int)S, (int)Skv, urange, (int)QT, topk, indices_out,
                                  (uint16_t*)topk_scores_out, st) == cudaSuccess
                ? LIDX_OK
                : LIDX_ERR_CUDA;

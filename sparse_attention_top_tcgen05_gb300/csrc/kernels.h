@@ -26,6 +26,8 @@ struct ScoreParams {
     const uint8_t* allowed;   // [B,S,Skv]
     uint16_t* out16;          // [B,S,Skv] bf16
     uint8_t* tilemap;         // [B, qtiles, ntk]: 1 where the block has a visible pair (written by the kernel)
+    int2* urange;             // nullable [B, qtiles]: key tiles [x, y) holding each query tile's visible
+                              // pairs (written by the kernel; (0, 0) when there are none)
     int ntk;                  // key tiles per row
     int vis_tma;              // 1: visibility flags staged by TMA (set by the launcher)
     const int32_t* idx_in;    // nullable [B,S,topk]: score these keys instead of selecting
@@ -61,8 +63,8 @@ cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, 
                              const int32_t* ks, const int32_t* ke, int topk, int32_t* out_idx,
                              float* out_sc, cudaStream_t stream);
 // selection over bf16 rows; -inf entries are not candidates (V4.1 scores)
-cudaError_t topk_rows_bf16_launch(const uint16_t* scores, int64_t rows, int Skv, int topk,
-                                  int32_t* out_idx, uint16_t* out_sc, cudaStream_t stream);
+cudaError_t topk_rows_bf16_launch(const uint16_t* scores, int64_t rows, int S, int Skv, const int2* urange,
+                                  int QT, int topk, int32_t* out_idx, uint16_t* out_sc, cudaStream_t stream);
 // backward through the selected entries (bwd.cu)
 struct BwdLaunch {
     const void* q;

@@ -118,15 +118,28 @@ __global__ void __launch_bounds__(kTopkRowThreads)
 
 // Selection over bf16 score rows in which -inf marks a key that is not
 // visible (the V4.1 scorer's output): candidates are the finite entries.
+// Top-k of bf16 V4.1 score rows, where -inf marks a key that is not visible:
+// candidates are the finite entries.  With `urange`, a row's keys are limited
+// to its query tile's range of key tiles, which holds all its visible keys.
 __global__ void __launch_bounds__(kTopkRowThreads)
-    topk_rows_bf16_kernel(const uint16_t* __restrict__ scores, int64_t rows, int Skv, int topk,
-                          int32_t* __restrict__ out_idx, uint16_t* __restrict__ out_sc) {
+    topk_rows_bf16_kernel(const uint16_t* __restrict__ scores, int64_t rows, int S, int Skv,
+                          const int2* __restrict__ urange, int QT, int topk, int32_t* __restrict__ out_idx,
+                          uint16_t* __restrict__ out_sc) {
     extern __shared__ uint8_t smem_raw[];
     TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
-    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x)
-        row_topk<kTopkRowThreads, true, uint16_t>(scores + r * (int64_t)Skv, 0, Skv, topk,
-                                                  out_idx + r * topk, out_sc + r * topk, sm,
-                                                  threadIdx.x, 1);
+    const int qtiles = (S + QT - 1) / QT;
+    for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
+        int lo = 0, hi = Skv;
+        if (urange) {
+            const int64_t b = r / S;
+            const int s = (int)(r - b * S);
+            const int2 kr = urange[b * qtiles + s / QT];
+            lo = kr.y > kr.x ? kr.x * 128 : 0;
+            hi = kr.y > kr.x ? min(kr.y * 128, Skv) : 0;
+        }
+        row_topk<kTopkRowThreads, true, uint16_t>(scores + r * (int64_t)Skv, lo, hi, topk, out_idx + r * topk,
+                                                  out_sc + r * topk, sm, threadIdx.x, 1);
+    }
 }
 
 template <class K>
@@ -157,14 +170,14 @@ cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, 
     return cudaGetLastError();
 }
 
-cudaError_t topk_rows_bf16_launch(const uint16_t* scores, int64_t rows, int Skv, int topk,
-                                  int32_t* out_idx, uint16_t* out_sc, cudaStream_t stream) {
+cudaError_t topk_rows_bf16_launch(const uint16_t* scores, int64_t rows, int S, int Skv, const int2* urange,
+                                  int QT, int topk, int32_t* out_idx, uint16_t* out_sc, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     int grid = 0, smem = 0;
     cudaError_t e = topk_grid(topk_rows_bf16_kernel, rows, &grid, &smem);
     if (e != cudaSuccess) return e;
-    topk_rows_bf16_kernel<<<(unsigned)grid, kTopkRowThreads, smem, stream>>>(scores, rows, Skv, topk,
-                                                                             out_idx, out_sc);
+    topk_rows_bf16_kernel<<<(unsigned)grid, kTopkRowThreads, smem, stream>>>(scores, rows, S, Skv, urange, QT,
+                                                                             topk, out_idx, out_sc);
     return cudaGetLastError();
 }
 

@@ -861,6 +861,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (lane == 0) {
                     sRec[slot] = r;
                     mbar_arrive(rec_full + slot);  // release: the record and the tile map row
+                    if (p.urange) p.urange[(size_t)b * p.qtiles + qt] = make_int2(r.x, r.y);
                 }
             }
             return true;

@@ -194,6 +194,8 @@ def test_topk_v41_packed_documents_full_size():
     (1, 64, 130, 1, 16, 0.9, 200),      # topk above every row's visible count
     (1, 33, 272, 4, 16, 0.0, 8),        # nothing visible
     (1, 40, 9000, 8, 32, 0.7, 4000),    # several candidate windows per row
+    (1, 60, 512, 8, 32, 0.4, 100),      # one warp a row, 129 to 256 visible keys
+    (1, 50, 1000, 16, 32, 0.6, 300),    # short span, too many visible keys for one warp
 ])
 def test_topk_v41_shapes(B, S, Skv, H, D, density, topk):
     g = np.random.default_rng(S + Skv + topk)
