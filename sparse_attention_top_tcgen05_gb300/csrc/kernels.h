@@ -33,6 +33,7 @@ struct ScoreParams {
     const int32_t* idx_in;    // nullable [B,S,topk]: score these keys instead of selecting
     uint64_t wait_ns;         // limit of every pipeline wait
     int debug_stall;          // 1: the TMA producer issues nothing (failure-detection tests)
+    int warp_rows;            // 1: each selection warp selects rows of its own (short rows)
     // filled by the launcher
     int num_units, qtiles, Skv_pad, swz;
 };

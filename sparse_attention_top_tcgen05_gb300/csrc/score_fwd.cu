@@ -931,17 +931,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ top-k
-        // Group g selects rows g, g+G, g+2G, ... of this CTA's sequence of units
-        // (QT rows each), so the load spreads evenly whatever QT is.  A group
-        // waits for every unit's rows in turn, even one holding none of its
-        // rows, so that it never tests a row-slot barrier two phases behind.
+        // Selector g selects rows g, g+G, g+2G, ... of this CTA's sequence of units
+        // (QT rows each), so the load spreads evenly whatever QT is.  A selector is
+        // a group of six warps, or, when every row spans at most kTopkShort keys, a
+        // single warp (G = 18).  A selector waits for every unit's rows in turn, even
+        // one holding none of its rows, so that it never tests a row-slot barrier
+        // two phases behind.
         const int ttid = threadIdx.x - 64 - kEpiThreads;
         const int grp = ttid / kTopkGroupThreads, gtid = ttid % kTopkGroupThreads;
+        const bool by_warp = p.warp_rows != 0;
+        const int nsel = by_warp ? kTopkWarps : kTopkGroups, sel_id = by_warp ? ttid / 32 : grp;
         TopkSmem& sTg = *(TopkSmem*)(smem + L.topk_off + grp * ((sizeof(TopkSmem) + 15) / 16 * 16));
         int i = 0, ucount = -1;
         Unit un{};
         bool ok = select;
-        for (int r = grp; ok; r += kTopkGroups) {
+        for (int r = sel_id; ok; r += nsel) {
             const int uc = r / QT, ql = r % QT;
             bool more = true;
             while (ok && ucount < uc) {
@@ -968,15 +972,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        ? p.logits + ((size_t)un.b * p.S + s) * p.Skv
                                        : p.scratch + ((size_t)blockIdx.x * 2 + rb) * p.scratch_stride_cta +
                                              (size_t)ql * p.Skv_pad;
-                if (p.idx_in)
+                if (by_warp) {  // one warp sorts the row in registers
+                    const int n = hi > lo ? hi - lo : 0;
+                    if (n <= 32)
+                        warp_topk_short<1, false, float>(row + lo, n, lo, p.topk, p.out_idx + orow,
+                                                         p.out_sc + orow, lane);
+                    else if (n <= 64)
+                        warp_topk_short<2, false, float>(row + lo, n, lo, p.topk, p.out_idx + orow,
+                                                         p.out_sc + orow, lane);
+                    else
+                        warp_topk_short<4, false, float>(row + lo, n, lo, p.topk, p.out_idx + orow,
+                                                         p.out_sc + orow, lane);
+                } else if (p.idx_in) {
                     row_gather<kTopkGroupThreads>(row, lo, hi, p.idx_in + orow, p.topk, p.out_idx + orow,
                                                   p.out_sc + orow, gtid, kTopkBar + grp);
-                else
+                } else {
                     row_topk<kTopkGroupThreads, false, float>(row, lo, hi, p.topk, p.out_idx + orow,
                                                               p.out_sc + orow, sTg, gtid,
                                                               kTopkBar + grp);  // ends with a group barrier
+                }
             }
-            if (gtid == 0) mbar_arrive(rows_empty + rb);  // this row's slot entry is free
+            if (by_warp) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rows_empty + rb);  // this row's slot entry is free
+            } else if (gtid == 0) {
+                mbar_arrive(rows_empty + rb);
+            }
         }
     }
 
@@ -1054,6 +1075,8 @@ int score_fwd_launch(ScoreLaunch& a) {
     ScoreParams& p = a.p;
     p.wait_ns = wait_limit_ns();
     p.debug_stall = debug_stall();
+    // rows of at most kTopkShort keys: each selection warp takes rows of its own
+    p.warp_rows = (p.idx_in == nullptr && p.Skv <= kTopkShort) ? 1 : 0;
     const int QT = kN / p.H;
     p.swz = (p.D % 64 == 0) ? 128 : (p.D % 32 == 0 ? 64 : 32);
     p.qtiles = (p.S + QT - 1) / QT;
