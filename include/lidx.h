@@ -261,10 +261,11 @@ int lidx_device_status(void* stream);
  * stalled pipeline ends the launch instead of hanging the GPU.
  *   lidx_set_wait_limit_ns  sets that limit for later launches (0 restores the
  *                           default of 2 s) and returns the previous one.
- *   lidx_debug_stall_producer  1: later launches of the scoring kernel load
- *                           nothing, so its waits run out (for tests of the
- *                           timeout path; outputs are then unspecified); 0:
- *                           normal operation.  Returns the previous setting.
+ *   lidx_debug_stall_producer  1: later launches of the scoring kernels (V4,
+ *                           V4.1) and of the backward's tensor-core kernels
+ *                           load nothing, so their waits run out (for tests of
+ *                           the timeout path; outputs are then unspecified);
+ *                           0: normal operation.  Returns the previous setting.
  * Both are process-wide and take effect at the next launch.
  */
 uint64_t lidx_set_wait_limit_ns(uint64_t ns);

@@ -67,6 +67,7 @@ struct BwdParams {
     int num_units;
     int U, CH, nchunks; // key-major: units per batch, query tiles per chunk, chunks
     uint64_t wait_ns;
+    int debug_stall;    // 1: the TMA producer issues nothing (failure-detection tests)
     int cpre[kBMaxChunks + 1];   // key-major: first unit of each chunk within a batch
 };
 
@@ -263,7 +264,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (lane == 0 && !p.debug_stall) {
             int kcount = 0, ucount = 0;
             bool ok = true;
             for (int i = 0; ok; ++i) {
@@ -903,6 +904,7 @@ cudaError_t bwd_launch(const BwdLaunch& a) {
     p.CH = pl.CH;
     p.nchunks = pl.nchunks;
     p.wait_ns = wait_limit_ns();
+    p.debug_stall = debug_stall();
     memcpy(p.cpre, pl.cpre, sizeof(int) * (pl.nchunks + 1));
     cudaError_t e;
     switch (a.H) {
