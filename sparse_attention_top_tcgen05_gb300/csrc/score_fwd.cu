@@ -1,10 +1,12 @@
-// score_fwd.cu -- V4 lightning-indexer forward on sm_103a tensor cores.
+// score_fwd.cu -- V4 and V4.1 lightning-indexer forward on sm_103a tensor cores.
 //
 // Computes, for a tile of query rows against every visible compressed key,
 //     logit[b,s,t] = sum_h w[s,b,h] * act(q[s,b,h,:] . k[t,b,:])
 // ("tilelang_indexer" page, V4IndexerFunction: SBHD layouts; "tilelang_indexer_fwd"
 // page, batched_indexer_fwd / indexer_fwd_interface / clean_logits_ /
-// _make_causal_cu_seqlens), then optionally the per-row top-k.
+// _make_causal_cu_seqlens), then optionally the per-row top-k; and the V4.1
+// bf16-rounded scores under an explicit visibility tensor ("deepseek_v41.indexer"
+// page, indexer_scores).
 //
 // Design (one persistent CTA per SM, warp-specialised):
 //   * The contraction is oriented keys x (query, head): UMMA M = 128 keys,
@@ -12,18 +14,24 @@
 //     so the head reduction sum_h w*act(x) is a per-thread loop over columns
 //     with no cross-lane traffic, and logits stores are 128 consecutive keys.
 //   * warp 0 lane 0: TMA producer.  The query tile [QT*H rows, D] stays resident
-//     for the whole key sweep; key tiles [128, D] stream through a 2-stage ring.
+//     for the whole key sweep (V4.1 keeps two); key tiles [128, D] stream through
+//     a 2-stage ring.
 //   * warp 1 lane 0: tcgen05.mma issuer into two 256-column fp32 accumulators
 //     (512 TMEM columns), so the MMA of tile i+1 overlaps the epilogue of tile i.
-//   * warps 2..9: epilogue, two warps per TMEM lane quadrant (128 columns each).
-//     tcgen05.ld -> act -> weighted head sum in fp32 -> mask -> store (logits)
-//     or stash in one of two per-CTA L2-resident row buffers.
-//   * warps 10..27: top-k in three groups of six warps (topk.cuh).  Group g
-//     takes rows g, g+3, ... of the CTA's query tiles from the row buffer the
-//     epilogue is not writing, so selection overlaps the next tile's key sweep.
-//   * Key tiles past the tile's last visible key are never loaded or multiplied.
-//     Query tiles are dealt to CTAs heaviest-first in a snake order; the next
-//     tile's queries are prefetched into L2 while the current one is swept.
+//   * V4: warps 2..9, epilogue, two warps per TMEM lane quadrant (128 columns
+//     each): tcgen05.ld -> act -> weighted head sum in fp32 -> mask -> store
+//     (logits) or stash in one of two per-CTA L2-resident row buffers.  Warps
+//     10..27 select, in three groups of six warps (topk.cuh), or one warp per row
+//     when rows are short: selector g takes rows g, g+G, ... of the CTA's query
+//     tiles from the row buffer the epilogue is not writing, so selection
+//     overlaps the next tile's key sweep.
+//   * V4.1: warps 2..17 (H <= 64) are the epilogue (bf16 rounding as the page
+//     states it); the remaining warps read `allowed`, publish each query tile's
+//     record of key tiles with a visible pair one unit ahead through a ring in
+//     shared memory, and write -inf over the blocks with none.
+//   * Key tiles with no visible pair are never loaded or multiplied.  Query
+//     tiles are dealt to CTAs heaviest-first in a snake order; the next tile's
+//     queries are prefetched into L2 while the current one is swept.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <string.h>
