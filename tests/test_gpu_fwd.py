@@ -154,6 +154,36 @@ def test_explicit_ranges_clean_and_unclean():
     assert np.array_equal(lg2[fin], lg.reshape(B * S, Skv)[fin])
 
 
+def test_explicit_ranges_short_rows_one_warp_each():
+    """Every row spans at most 128 keys (Skv = 120), so each selection warp takes
+    rows of its own; explicit ranges, including empty and clamped ones.  The fused
+    and materialised calls agree bit for bit, equal the exact top-k of the
+    kernel's own logits, and the oracle's within tolerance."""
+    g = np.random.default_rng(11)
+    S, B, H, D, Skv, topk = 700, 2, 32, 64, 120, 40
+    q = workloads.to_bf16(g.standard_normal((S, B, H, D)).astype(np.float32) / np.sqrt(D))
+    k = workloads.to_bf16(g.standard_normal((Skv, B, D)).astype(np.float32) / np.sqrt(D))
+    w = torch.from_numpy((g.standard_normal((S, B, H)) / np.sqrt(H)).astype(np.float32))
+    ks = g.integers(-5, Skv, S).astype(np.int32)
+    ke = (ks + g.integers(-3, 90, S)).astype(np.int32)
+    qd, kd, wd = cuda(q, k, w)
+    ksd, ked = torch.from_numpy(ks).to(DEV), torch.from_numpy(ke).to(DEV)
+    i1, s1, lg = lidx.lidx_indexer_fwd_ranges(qd, kd, wd, ksd, ked, topk, materialise_logits=True)
+    i2, s2, _ = lidx.lidx_indexer_fwd_ranges(qd, kd, wd, ksd, ked, topk)
+    torch.cuda.synchronize()
+    assert lidx.lidx_device_status() == 0
+    assert torch.equal(i1, i2) and torch.equal(s1, s2)
+    glg = lg.cpu().numpy().reshape(B * S, Skv)
+    olg = oracle.logits_rows(q, k, w, ks, ke)
+    assert_scores_close(glg, olg, "logits")
+    rs = np.arange(B * S) % S
+    eidx, esc = exact_selection_on(glg, ks, ke, topk, rs, oracle)
+    gidx, gsc = i1.cpu().numpy().reshape(B * S, topk), s1.cpu().numpy().reshape(B * S, topk)
+    assert np.array_equal(gidx, eidx)
+    assert np.array_equal(gsc.astype(np.float64), esc)
+    check_selection_vs_oracle(gidx, gsc, olg, ks, ke, topk, rs)
+
+
 def test_edge_cases():
     g = np.random.default_rng(4)
     # Skv = 0: every row is padding
