@@ -221,8 +221,10 @@ int lidx_indexer_topk_v41(const void* q, const void* k, const void* w,
  *   g = grad, x = q[s,b,h,:].k[t,b,:]:
  *     dw[s,b,h] += g*act(x);  dq[s,b,h,:] += g*w*act'(x)*k[t,b,:];
  *     dk[t,b,:] += sum_h g*w*act'(x)*q[s,b,h,:]        (ReLU'(0) = 0)
- *   dq fp32 [S,B,H,D], dk fp32 [Skv,B,D], dw fp32 [S,B,H]; all overwritten.
- *   grad_dtype must be 0 (fp32 outputs) in this build.
+ *   dq [S,B,H,D] and dk [Skv,B,D]: fp32 when grad_dtype = 0, bf16 (each the
+ *   fp32 result rounded to nearest even) when grad_dtype = 1; dw fp32 [S,B,H].
+ *   All are overwritten.  No atomic operation touches them: two calls on the
+ *   same inputs give identical bits.  Limit of this build: Skv <= 65536.
  *   workspace: lidx_workspace_bytes(LIDX_OP_INDEXER_BWD, ...) bytes.
  */
 int lidx_indexer_bwd(const void* q, const void* k, const float* w,
