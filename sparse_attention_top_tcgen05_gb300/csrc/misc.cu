@@ -116,17 +116,22 @@ __global__ void __launch_bounds__(kTopkRowThreads)
     }
 }
 
-// Selection over bf16 score rows in which -inf marks a key that is not
-// visible (the V4.1 scorer's output): candidates are the finite entries.
 // Top-k of bf16 V4.1 score rows, where -inf marks a key that is not visible:
 // candidates are the finite entries.  With `urange`, a row's keys are limited
 // to its query tile's range of key tiles, which holds all its visible keys.
-__global__ void __launch_bounds__(kTopkRowThreads)
+// Those spans are short, so a CTA of kTopkBf16Threads threads with a window of
+// kTopkBf16Cap members takes each row: more rows are in flight per SM than
+// with the full-size scratch, and a longer row takes more windows.
+constexpr int kTopkBf16Threads = 128;
+constexpr int kTopkBf16Cap = 1024;
+using TopkSmemBf16 = TopkSmemT<kTopkBf16Cap>;
+
+__global__ void __launch_bounds__(kTopkBf16Threads)
     topk_rows_bf16_kernel(const uint16_t* __restrict__ scores, int64_t rows, int S, int Skv,
                           const int2* __restrict__ urange, int QT, int topk, int32_t* __restrict__ out_idx,
                           uint16_t* __restrict__ out_sc) {
     extern __shared__ uint8_t smem_raw[];
-    TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
+    TopkSmemBf16& sm = *reinterpret_cast<TopkSmemBf16*>(smem_raw);
     const int qtiles = (S + QT - 1) / QT;
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         int lo = 0, hi = Skv;
@@ -137,24 +142,22 @@ __global__ void __launch_bounds__(kTopkRowThreads)
             lo = kr.y > kr.x ? kr.x * 128 : 0;
             hi = kr.y > kr.x ? min(kr.y * 128, Skv) : 0;
         }
-        row_topk<kTopkRowThreads, true, uint16_t>(scores + r * (int64_t)Skv, lo, hi, topk, out_idx + r * topk,
-                                                  out_sc + r * topk, sm, threadIdx.x, 1);
+        row_topk<kTopkBf16Threads, true, uint16_t>(scores + r * (int64_t)Skv, lo, hi, topk, out_idx + r * topk,
+                                                   out_sc + r * topk, sm, threadIdx.x, 1);
     }
 }
 
 template <class K>
-static cudaError_t topk_grid(K kern, int64_t rows, int* grid_out, int* smem_out) {
+static cudaError_t topk_grid(K kern, int threads, int smem, int64_t rows, int* grid_out) {
     const int sms = current_sms();
-    const int smem = (int)sizeof(TopkSmem);
     cudaError_t e = set_smem_attr((const void*)kern, smem);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTopkRowThreads, smem);
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
     if (per_sm < 1) per_sm = 1;
     int64_t grid = (int64_t)sms * per_sm;
     if (grid > rows) grid = rows;
     *grid_out = (int)grid;
-    *smem_out = smem;
     return cudaSuccess;
 }
 
@@ -162,8 +165,9 @@ cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, 
                              const int32_t* ks, const int32_t* ke, int topk, int32_t* out_idx,
                              float* out_sc, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    int grid = 0, smem = 0;
-    cudaError_t e = topk_grid(topk_rows_kernel, rows, &grid, &smem);
+    int grid = 0;
+    const int smem = (int)sizeof(TopkSmem);
+    cudaError_t e = topk_grid(topk_rows_kernel, kTopkRowThreads, smem, rows, &grid);
     if (e != cudaSuccess) return e;
     topk_rows_kernel<<<(unsigned)grid, kTopkRowThreads, smem, stream>>>(logits, rows, S, Skv, ratio, ks,
                                                                         ke, topk, out_idx, out_sc);
@@ -173,11 +177,12 @@ cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, 
 cudaError_t topk_rows_bf16_launch(const uint16_t* scores, int64_t rows, int S, int Skv, const int2* urange,
                                   int QT, int topk, int32_t* out_idx, uint16_t* out_sc, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
-    int grid = 0, smem = 0;
-    cudaError_t e = topk_grid(topk_rows_bf16_kernel, rows, &grid, &smem);
+    int grid = 0;
+    const int smem = (int)sizeof(TopkSmemBf16);
+    cudaError_t e = topk_grid(topk_rows_bf16_kernel, kTopkBf16Threads, smem, rows, &grid);
     if (e != cudaSuccess) return e;
-    topk_rows_bf16_kernel<<<(unsigned)grid, kTopkRowThreads, smem, stream>>>(scores, rows, S, Skv, urange, QT,
-                                                                             topk, out_idx, out_sc);
+    topk_rows_bf16_kernel<<<(unsigned)grid, kTopkBf16Threads, smem, stream>>>(scores, rows, S, Skv, urange, QT,
+                                                                              topk, out_idx, out_sc);
     return cudaGetLastError();
 }
 

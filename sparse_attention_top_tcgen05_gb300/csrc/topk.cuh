@@ -21,7 +21,7 @@
 //      monotone, so a lower bucket holds strictly larger scores.
 //   3. Histogram + exclusive scan give each bucket's first output position; the
 //      bucket holding position sel-1 is the last one needed.
-//   4. The needed buckets are taken in windows of at most kTopkCap members.  A
+//   4. The needed buckets are taken in windows of at most CAP members.  A
 //      window's members are scattered into shared memory as (score, key)
 //      pairs grouped by bucket.  A member of a bucket of at most kTopkSmall
 //      members is ranked against its bucket mates and written straight to its
@@ -31,7 +31,7 @@
 //      buckets are refined (step 5) or sorted in place by a bitonic network
 //      (one warp per bucket up to kTopkWarpSort members, else the whole group)
 //      and then written out.
-//   5. A single bucket with more than kTopkCap members becomes a new item
+//   5. A single bucket with more than CAP members becomes a new item
 //      over the exact value range of its members, bucketed by key; a few such
 //      refinements end in buckets that fit or in all-equal items.  Histogram
 //      and scatter combine the atomics of runs of one bucket (ties).
@@ -53,11 +53,10 @@ constexpr int kTopkWarpSort = 512;   // larger buckets up to this size: one warp
 constexpr int kTopkMaxKeys = 65536;  // visible span of a row (16-bit candidate offsets)
 constexpr int kTopkShort = 128;      // rows up to this span: one warp sorts the row in registers
 // Pending refined items are disjoint.  Those refined because they exceed a
-// window (> kTopkCap members) number at most 15; those refined by choice (a
-// bucket of more than kTopkWarpSort unequal members) at most kTopkStackOpt.
+// window (> CAP members) number fewer than kTopkMaxKeys / CAP; those refined by
+// choice (a bucket of more than kTopkWarpSort unequal members) at most
+// kTopkStackOpt.
 constexpr int kTopkStackOpt = 8;
-constexpr int kTopkStack = 16 + kTopkStackOpt;
-constexpr int kTopkMed = kTopkCap / (kTopkSmall + 1) + 1;
 constexpr int kTopkEqWords = 64;     // an all-equal bucket is ranked 2048 keys at a time
 
 // Histogram index of bucket b: one pad word per 32 buckets, so that lanes
@@ -73,12 +72,18 @@ struct TopkItem {
     int mode;          // 0: buckets linear in value, 1: linear in the order-preserving key
 };
 
-struct TopkSmem {
-    float cval[kTopkCap];         // window members, grouped by bucket
+// A group's scratch; CAP members of a row are held at a time (a window).  A
+// smaller CAP takes less shared memory and more windows on long rows.
+template <int CAP>
+struct TopkSmemT {
+    static constexpr int kCap = CAP;
+    static constexpr int kStack = kTopkMaxKeys / CAP + kTopkStackOpt;
+    static constexpr int kMed = CAP / (kTopkSmall + 1) + 1;
+    float cval[CAP];              // window members, grouped by bucket
     int start[kTopkHist];         // bucket offsets (padded); after the scatter, bucket ends
-    uint16_t cidx[kTopkCap];      // window members' keys (offsets from lo), same order as cval
-    TopkItem stack[kTopkStack];
-    int med[kTopkMed + 1];        // buckets of the window to sort (-1 - b: one dominant score)
+    uint16_t cidx[CAP];           // window members' keys (offsets from lo), same order as cval
+    TopkItem stack[kStack];
+    int med[kMed + 1];            // buckets of the window to sort (-1 - b: one dominant score)
     uint32_t eqbm[kTopkEqWords];  // members of an all-equal bucket, one bit per key of a chunk
     int eqpre[kTopkEqWords];      // set bits before each word of eqbm
     float red_max[8];
@@ -86,6 +91,7 @@ struct TopkSmem {
     int wsum[8];
     int bstar, nitems, nmed, whi, wbase, nbig, neq;
 };
+using TopkSmem = TopkSmemT<kTopkCap>;
 
 // ------------------------------------------------------------- element types
 template <class T>
@@ -213,8 +219,8 @@ __device__ __forceinline__ void row_pass_uniform(const T* r, int n, int tid, F&&
 }
 
 // Group-wide min/max/sum; all NT threads call with their partial values.
-template <int NT>
-__device__ __forceinline__ void group_minmax_count(float& vmin, float& vmax, int& cnt, TopkSmem& sm,
+template <int NT, class SM>
+__device__ __forceinline__ void group_minmax_count(float& vmin, float& vmax, int& cnt, SM& sm,
                                                    int tid, int bar_id) {
     constexpr int NW = NT / 32;
     const int lane = tid & 31, wid = tid >> 5;
@@ -286,9 +292,9 @@ __device__ __forceinline__ void bitonic_desc(float* sv, uint16_t* sj, int c, int
 
 // Emits, in index order, the first `sel` members of an all-equal item
 // (stable compaction with warp ballots; one barrier pair per NT entries).
-template <int NT, class T>
+template <int NT, class T, class SM>
 __device__ void topk_emit_equal(const T* r, int n, int lo, const TopkItem& it, int32_t* out_idx,
-                                T* out_sc, TopkSmem& sm, int tid, int bar_id) {
+                                T* out_sc, SM& sm, int tid, int bar_id) {
     constexpr int NW = NT / 32;
     const int lane = tid & 31, wid = tid >> 5;
     int done = 0;  // members emitted before this round (uniform)
@@ -325,9 +331,9 @@ __device__ void topk_emit_equal(const T* r, int n, int lo, const TopkItem& it, i
 // One work item of row_topk (see the method above).  All NT threads call it
 // with the same item; it may push refined items onto sm.stack (thread 0).
 // `cleared`: the histogram is already zero and visible to the group.
-template <int NT, class T>
+template <int NT, class T, class SM>
 __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cleared,
-                          int32_t* out_idx, T* out_sc, TopkSmem& sm, int tid, int bar_id) {
+                          int32_t* out_idx, T* out_sc, SM& sm, int tid, int bar_id) {
     constexpr int NW = NT / 32;
     constexpr int UNR = 4;  // 16-byte loads in flight per thread in each pass over the row
     const int lane = tid & 31, wid = tid >> 5;
@@ -400,22 +406,22 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
     named_bar_sync(bar_id, NT);
     const int bstar = sm.bstar;
     const bool any_big = sm.nbig > 0;  // some bucket is too large to rank pairwise
-    // 4. windows of consecutive buckets [w_lo, whi] with at most kTopkCap members.
+    // 4. windows of consecutive buckets [w_lo, whi] with at most SM::kCap members.
     // start[hidx(b)] is b's first position until b is scattered, its end after.
     int w_lo = 0;
     while (w_lo <= bstar) {
         if (tid == 0) {
             const int s_lo = sm.start[hidx(w_lo)];
             int whi;
-            if (sm.start[hidx(bstar + 1)] - s_lo <= kTopkCap) {
+            if (sm.start[hidx(bstar + 1)] - s_lo <= SM::kCap) {
                 whi = bstar;  // the rest fits in one window
-            } else if (sm.start[hidx(w_lo + 1)] - s_lo > kTopkCap) {
+            } else if (sm.start[hidx(w_lo + 1)] - s_lo > SM::kCap) {
                 whi = -1;  // one bucket too large for a window
             } else {
                 int a = w_lo, b = bstar;  // largest whi in [a, b] whose window fits
                 while (a < b) {
                     const int mid = (a + b + 1) >> 1;
-                    if (sm.start[hidx(mid + 1)] - s_lo <= kTopkCap)
+                    if (sm.start[hidx(mid + 1)] - s_lo <= SM::kCap)
                         a = mid;
                     else
                         b = mid - 1;
@@ -450,7 +456,7 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
                 const int want = it.sel - wbase;
                 ch.sel = want < bc ? want : bc;
                 ch.mode = 1;
-                if (sm.nitems < kTopkStack) sm.stack[sm.nitems++] = ch;
+                if (sm.nitems < SM::kStack) sm.stack[sm.nitems++] = ch;
                 sm.start[hidx(b0)] = bend;  // as if scattered: b0 + 1 finds its start
             }
             named_bar_sync(bar_id, NT);
@@ -493,7 +499,7 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
             for (int b = w_lo + tid; b <= whi; b += NT)
                 if (sm.start[hidx(b)] - bbegin(b) > kTopkSmall) {
                     const int k = atomicAdd(&sm.nmed, 1);
-                    if (k < kTopkMed) sm.med[k] = b;
+                    if (k < SM::kMed) sm.med[k] = b;
                 }
         // rank each member of a small bucket [begin(b), end(b)) and write it out
         const int wend = sm.start[hidx(whi)] - wbase;
@@ -525,7 +531,7 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
         if (any_big) {
             // sort the large buckets in place, then write them out
             named_bar_sync(bar_id, NT);
-            const int nmed = sm.nmed < kTopkMed ? sm.nmed : kTopkMed;
+            const int nmed = sm.nmed < SM::kMed ? sm.nmed : SM::kMed;
             // A bucket in which all but at most kTopkSmall members hold one score
             // v0 is ranked in place (code -1 - b): members above v0 first, then
             // those equal to v0 in key order, then those below.  One of more
@@ -757,9 +763,9 @@ __device__ void warp_topk_short(const T* r, int n, int lo, int topk, int32_t* ou
 // of the group must call it with identical scalar arguments, after a group
 // barrier that ends any earlier use of `sm`; hi - lo must not exceed
 // kTopkMaxKeys.  The row is global (L2-resident) and read several times.
-template <int NT, bool SKIP_NINF, class T>
+template <int NT, bool SKIP_NINF, class T, class SM>
 __device__ void row_topk(const T* row, int lo, int hi, int topk, int32_t* out_idx, T* out_sc,
-                         TopkSmem& sm, int tid, int bar_id) {
+                         SM& sm, int tid, int bar_id) {
     static_assert(NT % 32 == 0 && NT <= 256, "group size");
     const int n = hi > lo ? hi - lo : 0;
     const float ninf = __int_as_float(0xff800000), pinf = __int_as_float(0x7f800000);
