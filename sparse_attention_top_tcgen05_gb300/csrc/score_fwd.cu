@@ -37,6 +37,8 @@
 #include <string.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 #include "topk.cuh"
@@ -53,8 +55,10 @@ constexpr int kTopkThreads = 32 * kTopkWarps;
 constexpr int kThreads = 64 + kEpiThreads + kTopkThreads;
 constexpr int kEpiBar = 1;         // named barrier id of the epilogue group
 constexpr int kTopkBar = 2;        // named barrier ids of the selection groups: 2, 3, 4
-constexpr int kTopkGroups = 3;     // rows selected concurrently
+constexpr int kTopkGroups = 3;     // rows selected concurrently (the scratch is sized for these)
 constexpr int kTopkGroupThreads = kTopkThreads / kTopkGroups;
+constexpr int kTopkGroupsShort = 6;   // rows selected concurrently when Skv <= kTopkShortCap
+constexpr int kTopkShortCap = 1024;   // their window: each group's scratch is a sixth of the region
 constexpr int kVisStages = 4;      // V4.1: ring of staged visibility blocks
 constexpr int kRecSlots = 4;       // V4.1: ring of per-unit visibility records
 constexpr int kFillBar = 5;        // V4.1: named barrier id of the visibility / fill warps
@@ -311,7 +315,9 @@ struct RecBuild {
     uint32_t bits[kRecBitTiles / 32];
 };
 
-template <int H, bool V41>
+// SEL (V4 only): the selection runs kTopkGroupsShort groups with a window of
+// kTopkShortCap members, for rows of at most that many keys.
+template <int H, bool V41, bool SEL>
 __global__ void __launch_bounds__(kThreads, 1)
     score_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tma, const ScoreParams p) {
@@ -945,11 +951,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // single warp (G = 18).  A selector waits for every unit's rows in turn, even
         // one holding none of its rows, so that it never tests a row-slot barrier
         // two phases behind.
+        constexpr int NG = SEL ? kTopkGroupsShort : kTopkGroups;  // groups
+        constexpr int GT = kTopkThreads / NG;                      // threads of a group
+        using SMT = typename std::conditional<SEL, TopkSmemT<kTopkShortCap>, TopkSmem>::type;
+        constexpr uint32_t kGroupBytes = (sizeof(SMT) + 15) / 16 * 16;
+        static_assert(NG * kGroupBytes <= kTopkGroups * ((sizeof(TopkSmem) + 15) / 16 * 16),
+                      "selection groups exceed the scratch region");
+        static_assert(kTopkBar + NG <= 16, "named barrier ids");
         const int ttid = threadIdx.x - 64 - kEpiThreads;
-        const int grp = ttid / kTopkGroupThreads, gtid = ttid % kTopkGroupThreads;
+        const int grp = ttid / GT, gtid = ttid % GT;
         const bool by_warp = p.warp_rows != 0;
-        const int nsel = by_warp ? kTopkWarps : kTopkGroups, sel_id = by_warp ? ttid / 32 : grp;
-        TopkSmem& sTg = *(TopkSmem*)(smem + L.topk_off + grp * ((sizeof(TopkSmem) + 15) / 16 * 16));
+        const int nsel = by_warp ? kTopkWarps : NG, sel_id = by_warp ? ttid / 32 : grp;
+        SMT& sTg = *(SMT*)(smem + L.topk_off + grp * kGroupBytes);
         int i = 0, ucount = -1;
         Unit un{};
         bool ok = select;
@@ -992,10 +1005,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         warp_topk_short<4, false, float>(row + lo, n, lo, p.topk, p.out_idx + orow,
                                                          p.out_sc + orow, lane);
                 } else if (p.idx_in) {
-                    row_gather<kTopkGroupThreads>(row, lo, hi, p.idx_in + orow, p.topk, p.out_idx + orow,
+                    row_gather<GT>(row, lo, hi, p.idx_in + orow, p.topk, p.out_idx + orow,
                                                   p.out_sc + orow, gtid, kTopkBar + grp);
                 } else {
-                    row_topk<kTopkGroupThreads, false, float>(row, lo, hi, p.topk, p.out_idx + orow,
+                    row_topk<GT, false, float>(row, lo, hi, p.topk, p.out_idx + orow,
                                                               p.out_sc + orow, sTg, gtid,
                                                               kTopkBar + grp);  // ends with a group barrier
                 }
@@ -1044,28 +1057,28 @@ static int encode_maps(const ScoreLaunch& a, CUtensorMap* mq, CUtensorMap* mk) {
     return 0;
 }
 
-template <int H, bool V41>
+template <int H, bool V41, bool SEL>
 static cudaError_t launch_h(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& ma, int smem, int grid) {
-    auto kern = score_fwd_kernel<H, V41>;
+    auto kern = score_fwd_kernel<H, V41, SEL>;
     cudaError_t e = set_smem_attr((const void*)kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, ma, a.p);
     return cudaGetLastError();
 }
 
-template <bool V41>
+template <bool V41, bool SEL>
 static cudaError_t launch_any(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& ma, int smem, int grid) {
     switch (a.p.H) {
-        case 1: return launch_h<1, V41>(a, mq, mk, ma, smem, grid);
-        case 2: return launch_h<2, V41>(a, mq, mk, ma, smem, grid);
-        case 4: return launch_h<4, V41>(a, mq, mk, ma, smem, grid);
-        case 8: return launch_h<8, V41>(a, mq, mk, ma, smem, grid);
-        case 16: return launch_h<16, V41>(a, mq, mk, ma, smem, grid);
-        case 32: return launch_h<32, V41>(a, mq, mk, ma, smem, grid);
-        case 64: return launch_h<64, V41>(a, mq, mk, ma, smem, grid);
-        case 128: return launch_h<128, V41>(a, mq, mk, ma, smem, grid);
+        case 1: return launch_h<1, V41, SEL>(a, mq, mk, ma, smem, grid);
+        case 2: return launch_h<2, V41, SEL>(a, mq, mk, ma, smem, grid);
+        case 4: return launch_h<4, V41, SEL>(a, mq, mk, ma, smem, grid);
+        case 8: return launch_h<8, V41, SEL>(a, mq, mk, ma, smem, grid);
+        case 16: return launch_h<16, V41, SEL>(a, mq, mk, ma, smem, grid);
+        case 32: return launch_h<32, V41, SEL>(a, mq, mk, ma, smem, grid);
+        case 64: return launch_h<64, V41, SEL>(a, mq, mk, ma, smem, grid);
+        case 128: return launch_h<128, V41, SEL>(a, mq, mk, ma, smem, grid);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1101,7 +1114,9 @@ int score_fwd_launch(ScoreLaunch& a) {
     if (p.H < 1 || p.H > 128 || (p.H & (p.H - 1))) return -2;
     CUtensorMap unused;
     memset(&unused, 0, sizeof unused);
-    const cudaError_t e = launch_any<false>(a, mq, mk, unused, smem, grid);
+    // rows of at most kTopkShortCap keys: more selection groups with smaller windows
+    const cudaError_t e = p.Skv <= kTopkShortCap ? launch_any<false, true>(a, mq, mk, unused, smem, grid)
+                                                 : launch_any<false, false>(a, mq, mk, unused, smem, grid);
     a.launched = grid;
     return e == cudaSuccess ? 0 : -1;
 }
@@ -1154,7 +1169,7 @@ int score_v41_launch(ScoreLaunch& a) {
     }
     int smem = (int)smem_layout(p.D).total;
     if (smem < 120 * 1024) smem = 120 * 1024;
-    const cudaError_t e = launch_any<true>(a, mq, mk, ma, smem, grid);
+    const cudaError_t e = launch_any<true, false>(a, mq, mk, ma, smem, grid);
     a.launched = grid;
     return e == cudaSuccess ? 0 : -1;
 }
