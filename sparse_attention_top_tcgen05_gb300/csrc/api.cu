@@ -318,11 +318,15 @@ size_t lidx_workspace_bytes(int op, int64_t B, int64_t S, int64_t Skv, int H, in
 
 int lidx_device_status(void* stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LIDX_ERR_CUDA;
-    int a = status_score_fwd(1), b = status_misc(1), c = status_bwd(1);
-    if (a < 0 || b < 0 || c < 0) return LIDX_ERR_CUDA;
-    if (a) return a;
-    if (b) return b;
-    return c;
+    // one status word per translation unit with kernels; every one is read (and cleared)
+    const int st[] = {status_score_v4(1), status_score_v4_short(1), status_score_v41(1), status_misc(1),
+                      status_bwd(1)};
+    int first = 0;
+    for (int v : st) {
+        if (v < 0) return LIDX_ERR_CUDA;
+        if (v != 0 && first == 0) first = v;
+    }
+    return first;
 }
 
 uint64_t lidx_set_wait_limit_ns(uint64_t ns) {

@@ -53,6 +53,13 @@ int encode_tiled(CUtensorMap* map, CUtensorMapDataType dtype, int rank, void* ad
                  const cuuint32_t* elem_strides, CUtensorMapSwizzle swizzle);
 
 int score_fwd_launch(ScoreLaunch& a);
+// the scoring kernels of one configuration for the call's head count
+cudaError_t score_launch_v4(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                            const CUtensorMap& ma, int smem, int grid);
+cudaError_t score_launch_v4_short(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                                  const CUtensorMap& ma, int smem, int grid);
+cudaError_t score_launch_v41(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                             const CUtensorMap& ma, int smem, int grid);
 int score_v41_launch(ScoreLaunch& a);
 int score_query_tile(int H);  // query rows per tile for H heads
 size_t score_scratch_bytes(int64_t S, int64_t Skv, int H, int num_sms);
@@ -105,7 +112,9 @@ uint64_t wait_limit_ns();                             // limit of every pipeline
 int debug_stall();                                    // failure-detection test switch
 
 // per-TU status readers (see LIDX_STATUS_READER): value, or -1 on a CUDA error
-int status_score_fwd(int clear);
+int status_score_v4(int clear);        // status words of the scoring kernels' units
+int status_score_v4_short(int clear);
+int status_score_v41(int clear);
 int status_misc(int clear);
 int status_bwd(int clear);
 
