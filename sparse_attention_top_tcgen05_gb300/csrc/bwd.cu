@@ -684,6 +684,8 @@ __global__ void bwd_reduce_kernel(const float* __restrict__ part, int B, int Skv
         const int t = (int)(bt % Skv), b = (int)(bt / Skv);
         const int kt = t / kBT, tl = t % kBT;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // one accumulator in chunk order; the unrolling only keeps loads in flight
+#pragma unroll 8
         for (int c = bwd_c0(causal != 0, kt, ratio, QT, qtiles, CH, nchunks); c < nchunks; ++c) {
             const int u = b * U + tab.cpre[c] + kt;
             const float4 v = *reinterpret_cast<const float4*>(part + ((size_t)u * kBT + tl) * Dp + d4);
@@ -861,7 +863,7 @@ cudaError_t bwd_launch(const BwdLaunch& a) {
             cudaError_t e = set_smem_attr((const void*)bwd_scatter_kernel, smem);
             if (e != cudaSuccess) return e;
         }
-        int64_t grid = (int64_t)a.num_sms * 4;
+        int64_t grid = (int64_t)a.num_sms * 8;  // eight rows in flight per SM
         if (grid > rows) grid = rows;
         bwd_scatter_kernel<<<(unsigned)grid, kScatterThreads, smem, a.stream>>>(
             a.idx, a.grad, a.B, a.S, a.Skv, pl.Skv_pad, a.ratio, a.ks, a.ke, a.topk, G, in_smem);
