@@ -107,6 +107,7 @@ def test_packed_documents_full_size_sampled():
     (2, 100, 400, 8, 64, 0.3),
     (1, 70, 208, 16, 32, 0.0005),
     (1, 33, 272, 4, 16, 0.0),
+    (2, 300, 200, 2, 32, 0.4),     # 128 query rows a unit: flags read from global memory
 ])
 def test_shapes_random_visibility(B, S, Skv, H, D, density):
     g = np.random.default_rng(S + Skv)
