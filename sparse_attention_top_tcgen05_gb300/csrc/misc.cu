@@ -124,7 +124,8 @@ __global__ void __launch_bounds__(kTopkRowThreads)
 // with the full-size scratch, and a longer row takes more windows.
 constexpr int kTopkBf16Threads = 128;
 constexpr int kTopkBf16Cap = 1024;
-using TopkSmemBf16 = TopkSmemT<kTopkBf16Cap>;
+constexpr int kTopkBf16Buckets = 384;  // a short span needs fewer buckets to split it
+using TopkSmemBf16 = TopkSmemT<kTopkBf16Cap, kTopkBf16Buckets>;
 
 __global__ void __launch_bounds__(kTopkBf16Threads)
     topk_rows_bf16_kernel(const uint16_t* __restrict__ scores, int64_t rows, int S, int Skv,

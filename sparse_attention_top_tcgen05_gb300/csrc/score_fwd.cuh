@@ -60,6 +60,7 @@ constexpr int kTopkGroups = 3;     // rows selected concurrently (the scratch is
 constexpr int kTopkGroupThreads = kTopkThreads / kTopkGroups;
 constexpr int kTopkGroupsShort = 6;   // rows selected concurrently when Skv <= kTopkShortCap
 constexpr int kTopkShortCap = 1024;   // their window: each group's scratch is a sixth of the region
+constexpr int kTopkShortBuckets = 768; // and their value buckets: fewer suffice for a span that short
 constexpr int kVisStages = 4;      // V4.1: ring of staged visibility blocks
 constexpr int kRecSlots = 4;       // V4.1: ring of per-unit visibility records
 constexpr int kFillBar = 5;        // V4.1: named barrier id of the visibility / fill warps
@@ -954,7 +955,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // two phases behind.
         constexpr int NG = SEL ? kTopkGroupsShort : kTopkGroups;  // groups
         constexpr int GT = kTopkThreads / NG;                      // threads of a group
-        using SMT = typename std::conditional<SEL, TopkSmemT<kTopkShortCap>, TopkSmem>::type;
+        using SMT = typename std::conditional<SEL, TopkSmemT<kTopkShortCap, kTopkShortBuckets>, TopkSmem>::type;
         constexpr uint32_t kGroupBytes = (sizeof(SMT) + 15) / 16 * 16;
         static_assert(NG * kGroupBytes <= kTopkGroups * ((sizeof(TopkSmem) + 15) / 16 * 16),
                       "selection groups exceed the scratch region");

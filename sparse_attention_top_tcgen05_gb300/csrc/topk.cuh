@@ -63,7 +63,7 @@ constexpr int kTopkEqWords = 64;     // an all-equal bucket is ranked 2048 keys 
 // reading runs of consecutive buckets hit distinct banks.  Slot hidx(NB)
 // holds the item's member count.
 __device__ __forceinline__ int hidx(int b) { return b + (b >> 5); }
-constexpr int kTopkHist = kTopkBuckets + kTopkBuckets / 32 + 2;
+
 
 struct TopkItem {
     float lo_v, hi_v;  // members: visible scores v with lo_v <= v <= hi_v
@@ -74,13 +74,15 @@ struct TopkItem {
 
 // A group's scratch; CAP members of a row are held at a time (a window).  A
 // smaller CAP takes less shared memory and more windows on long rows.
-template <int CAP>
+template <int CAP, int NB = kTopkBuckets>
 struct TopkSmemT {
     static constexpr int kCap = CAP;
+    static constexpr int kNB = NB;                       // value buckets of an item
+    static constexpr int kHist = NB + NB / 32 + 2;       // padded histogram slots
     static constexpr int kStack = kTopkMaxKeys / CAP + kTopkStackOpt;
     static constexpr int kMed = CAP / (kTopkSmall + 1) + 1;
     float cval[CAP];              // window members, grouped by bucket
-    int start[kTopkHist];         // bucket offsets (padded); after the scatter, bucket ends
+    int start[kHist];             // bucket offsets (padded); after the scatter, bucket ends
     uint16_t cidx[CAP];           // window members' keys (offsets from lo), same order as cval
     TopkItem stack[kStack];
     int med[kMed + 1];            // buckets of the window to sort (-1 - b: one dominant score)
@@ -122,6 +124,7 @@ __device__ __forceinline__ bool topk_before(float v, int j, float w, int k) {
     return v > w || (v == w && j < k);
 }
 
+template <int NB>
 struct TopkMap {
     int mode;
     float hi_v, scale;  // mode 0
@@ -131,23 +134,24 @@ struct TopkMap {
         if (mode == 0) {
             const float x = __fmul_rn(__fsub_rn(hi_v, v), scale);
             const int b = (int)x;  // x >= 0; the conversion saturates
-            return b < kTopkBuckets ? b : kTopkBuckets - 1;
+            return b < NB ? b : NB - 1;
         }
         const uint64_t d = (uint64_t)(khi - topk_okey(v));
         return (int)((d * mul) >> 32);  // d < range, mul <= NB*2^32/range: < NB
     }
 };
 
-__device__ __forceinline__ TopkMap topk_map(const TopkItem& it) {
-    TopkMap m;
+template <int NB>
+__device__ __forceinline__ TopkMap<NB> topk_map(const TopkItem& it) {
+    TopkMap<NB> m;
     m.mode = it.mode;
     m.hi_v = it.hi_v;
-    float scale = (float)kTopkBuckets / __fsub_rn(it.hi_v, it.lo_v);
+    float scale = (float)NB / __fsub_rn(it.hi_v, it.lo_v);
     if (!(scale < __int_as_float(0x7f800000))) scale = 0.f;  // range overflowed or underflowed
     m.scale = scale;
     m.khi = topk_okey(it.hi_v);
     const uint64_t range = (uint64_t)(m.khi - topk_okey(it.lo_v)) + 1;
-    m.mul = (((uint64_t)kTopkBuckets) << 32) / range;
+    m.mul = (((uint64_t)NB) << 32) / range;
     return m;
 }
 
@@ -343,12 +347,12 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
         topk_emit_equal<NT, T>(r, n, lo, it, out_idx, out_sc, sm, tid, bar_id);
         return;
     }
-    const TopkMap bm = topk_map(it);
+    const auto bm = topk_map<SM::kNB>(it);
     // 2. histogram
     if (!cleared) {
-        for (int i = tid; i < kTopkHist; i += NT) sm.start[i] = 0;
+        for (int i = tid; i < SM::kHist; i += NT) sm.start[i] = 0;
         if (tid == 0) {
-            sm.bstar = kTopkBuckets - 1;  // set by the scan unless scores are not finite
+            sm.bstar = SM::kNB - 1;  // set by the scan unless scores are not finite
             sm.nbig = 0;
         }
         named_bar_sync(bar_id, NT);
@@ -372,8 +376,8 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
     named_bar_sync(bar_id, NT);
     // 3. exclusive scan: thread tid owns buckets [tid*PER, tid*PER + PER)
     {
-        constexpr int PER = kTopkBuckets / NT;
-        static_assert(kTopkBuckets % NT == 0 && PER >= 1, "bucket split");
+        constexpr int PER = SM::kNB / NT;
+        static_assert(SM::kNB % NT == 0 && PER >= 1, "bucket split");
         int c[PER];
         int local = 0, big = 0;
 #pragma unroll
@@ -401,7 +405,7 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
             if (base < it.sel && base + c[i] >= it.sel) sm.bstar = b;
             base += c[i];
         }
-        if (tid == NT - 1) sm.start[hidx(kTopkBuckets)] = base;  // member count
+        if (tid == NT - 1) sm.start[hidx(SM::kNB)] = base;  // member count
     }
     named_bar_sync(bar_id, NT);
     const int bstar = sm.bstar;
@@ -794,10 +798,10 @@ __device__ void row_topk(const T* row, int lo, int hi, int topk, int32_t* out_id
             ++cnt;
         });
     // clear the first item's histogram under the same barrier
-    for (int i = tid; i < kTopkHist; i += NT) sm.start[i] = 0;
+    for (int i = tid; i < SM::kHist; i += NT) sm.start[i] = 0;
     if (tid == 0) {
         sm.nitems = 0;
-        sm.bstar = kTopkBuckets - 1;
+        sm.bstar = SM::kNB - 1;
         sm.nbig = 0;
     }
     group_minmax_count<NT>(vmin, vmax, cnt, sm, tid, bar_id);
