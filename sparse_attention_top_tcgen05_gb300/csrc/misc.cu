@@ -90,14 +90,17 @@ cudaError_t copy_pad_launch(int64_t n, const int32_t* in, int32_t* idx, float* s
 }
 
 // Standalone selection: each CTA (kTopkRowThreads threads) takes rows in turn.
+// Its scratch has a bitmap of 4096 keys, so an all-equal bucket of a row of up
+// to 4096 keys is ranked in one chunk.
 constexpr int kTopkRowThreads = 256;
+using TopkSmemRows = TopkSmemT<kTopkCap, kTopkBuckets, 128>;
 
 __global__ void __launch_bounds__(kTopkRowThreads)
     topk_rows_kernel(const float* __restrict__ logits, int64_t rows, int S, int Skv, int ratio,
                      const int32_t* __restrict__ ks, const int32_t* __restrict__ ke, int topk,
                      int32_t* __restrict__ out_idx, float* __restrict__ out_sc) {
     extern __shared__ uint8_t smem_raw[];
-    TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
+    TopkSmemRows& sm = *reinterpret_cast<TopkSmemRows*>(smem_raw);
     for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
         const int s = (int)(r % S);
         int lo, hi;
@@ -125,7 +128,7 @@ __global__ void __launch_bounds__(kTopkRowThreads)
 constexpr int kTopkBf16Threads = 128;
 constexpr int kTopkBf16Cap = 1024;
 constexpr int kTopkBf16Buckets = 384;  // a short span needs fewer buckets to split it
-using TopkSmemBf16 = TopkSmemT<kTopkBf16Cap, kTopkBf16Buckets>;
+using TopkSmemBf16 = TopkSmemT<kTopkBf16Cap, kTopkBf16Buckets, 128>;
 
 __global__ void __launch_bounds__(kTopkBf16Threads)
     topk_rows_bf16_kernel(const uint16_t* __restrict__ scores, int64_t rows, int S, int Skv,
@@ -167,7 +170,7 @@ cudaError_t topk_rows_launch(const float* logits, int64_t rows, int S, int Skv, 
                              float* out_sc, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     int grid = 0;
-    const int smem = (int)sizeof(TopkSmem);
+    const int smem = (int)sizeof(TopkSmemRows);
     cudaError_t e = topk_grid(topk_rows_kernel, kTopkRowThreads, smem, rows, &grid);
     if (e != cudaSuccess) return e;
     topk_rows_kernel<<<(unsigned)grid, kTopkRowThreads, smem, stream>>>(logits, rows, S, Skv, ratio, ks,

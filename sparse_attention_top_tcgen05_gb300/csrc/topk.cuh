@@ -57,7 +57,8 @@ constexpr int kTopkShort = 128;      // rows up to this span: one warp sorts the
 // choice (a bucket of more than kTopkWarpSort unequal members) at most
 // kTopkStackOpt.
 constexpr int kTopkStackOpt = 8;
-constexpr int kTopkEqWords = 64;     // an all-equal bucket is ranked 2048 keys at a time
+constexpr int kTopkEqWords = 64;     // default bitmap: an all-equal bucket is ranked 2048 keys at a time
+constexpr int kEqOnly = 1 << 20;     // flag in a large bucket's code: all its members hold one score
 
 // Histogram index of bucket b: one pad word per 32 buckets, so that lanes
 // reading runs of consecutive buckets hit distinct banks.  Slot hidx(NB)
@@ -74,11 +75,13 @@ struct TopkItem {
 
 // A group's scratch; CAP members of a row are held at a time (a window).  A
 // smaller CAP takes less shared memory and more windows on long rows.
-template <int CAP, int NB = kTopkBuckets>
+template <int CAP, int NB = kTopkBuckets, int EQW = kTopkEqWords>
 struct TopkSmemT {
     static constexpr int kCap = CAP;
     static constexpr int kNB = NB;                       // value buckets of an item
     static constexpr int kHist = NB + NB / 32 + 2;       // padded histogram slots
+    static constexpr int kEqWords = EQW;                 // bitmap words: 32*EQW keys a chunk
+    static_assert(EQW % 32 == 0 && EQW >= kTopkSmall && EQW <= 256, "bitmap words");
     static constexpr int kStack = kTopkMaxKeys / CAP + kTopkStackOpt;
     static constexpr int kMed = CAP / (kTopkSmall + 1) + 1;
     float cval[CAP];              // window members, grouped by bucket
@@ -86,8 +89,8 @@ struct TopkSmemT {
     uint16_t cidx[CAP];           // window members' keys (offsets from lo), same order as cval
     TopkItem stack[kStack];
     int med[kMed + 1];            // buckets of the window to sort (-1 - b: one dominant score)
-    uint32_t eqbm[kTopkEqWords];  // members of an all-equal bucket, one bit per key of a chunk
-    int eqpre[kTopkEqWords];      // set bits before each word of eqbm
+    uint32_t eqbm[EQW];           // members of an all-equal bucket, one bit per key of a chunk
+    int eqpre[EQW];               // set bits before each word of eqbm (within its warp's 32)
     float red_max[8];
     float red_min[8];
     int wsum[8];
@@ -562,7 +565,7 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
                 }
                 if (lane == 0) {
                     if (ne <= kTopkSmall) {
-                        sm.med[i] = -1 - b;
+                        sm.med[i] = -1 - b - (ne == 0 ? kEqOnly : 0);
                     } else if (e0 - s0 > kTopkWarpSort) {
                         const int slot = atomicAdd(&sm.nitems, 1);
                         if (slot < kTopkStackOpt) {
@@ -586,17 +589,20 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
             for (int i = 0; i < nmed; ++i) {
                 const int code = sm.med[i];
                 if (code >= 0 || code == INT_MIN) continue;
-                const int b = -1 - code;
+                const bool only = -1 - code >= kEqOnly;  // every member holds v0
+                const int b = (-1 - code) & (kEqOnly - 1);
                 const int s0 = bbegin(b) - wbase, e0 = sm.start[hidx(b)] - wbase;
                 const int bb = bbegin(b);  // item-local position of the bucket
                 const float v0 = sm.cval[s0];
                 // members off the dominant score (at most kTopkSmall): list, then rank
-                for (int p = s0 + tid; p < e0; p += NT)
-                    if (sm.cval[p] != v0) sm.eqpre[atomicAdd(&sm.neq, 1)] = p;
-                named_bar_sync(bar_id, NT);
-                const int neq = sm.neq;
-                int gt = 0;
-                for (int x = 0; x < neq; ++x) gt += sm.cval[sm.eqpre[x]] > v0;
+                int neq = 0, gt = 0;
+                if (!only) {
+                    for (int p = s0 + tid; p < e0; p += NT)
+                        if (sm.cval[p] != v0) sm.eqpre[atomicAdd(&sm.neq, 1)] = p;
+                    named_bar_sync(bar_id, NT);
+                    neq = sm.neq;
+                    for (int x = 0; x < neq; ++x) gt += sm.cval[sm.eqpre[x]] > v0;
+                }
                 if (tid < neq) {
                     const int p = sm.eqpre[tid];
                     const float v = sm.cval[p];
@@ -614,19 +620,21 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
                         out_sc[it.base + pos] = topk_from_f<T>(v);
                     }
                 }
-                named_bar_sync(bar_id, NT);  // the list is read; eqpre is reused below
+                if (!only) named_bar_sync(bar_id, NT);  // the list is read; eqpre is reused below
                 // members equal to v0: rank of key j = set bits below j in a bitmap
+                constexpr int EQW = SM::kEqWords, EQK = 32 * EQW;
+                static_assert(NT >= EQW, "one thread per bitmap word");
                 int before = 0;  // such members in earlier chunks
-                for (int c0 = 0; c0 < n; c0 += 32 * kTopkEqWords) {
-                    for (int x = tid; x < kTopkEqWords; x += NT) sm.eqbm[x] = 0u;
+                for (int c0 = 0; c0 < n; c0 += EQK) {
+                    for (int x = tid; x < EQW; x += NT) sm.eqbm[x] = 0u;
                     named_bar_sync(bar_id, NT);
                     for (int p = s0 + tid; p < e0; p += NT) {
                         const int j = (int)sm.cidx[p] - c0;
-                        if (sm.cval[p] == v0 && j >= 0 && j < 32 * kTopkEqWords)
+                        if ((only || sm.cval[p] == v0) && j >= 0 && j < EQK)
                             atomicOr(&sm.eqbm[j >> 5], 1u << (j & 31));
                     }
                     named_bar_sync(bar_id, NT);
-                    if (tid < kTopkEqWords) {
+                    if (tid < EQW) {
                         const int cnt = __popc(sm.eqbm[tid]);
                         int incl = cnt;
 #pragma unroll
@@ -638,12 +646,18 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
                         if (lane == 31) sm.wsum[wid] = incl;
                     }
                     named_bar_sync(bar_id, NT);
-                    static_assert(kTopkEqWords == 64 && NT >= 64, "two warps scan the bitmap");
+                    int wpre[EQW / 32];  // set bits in the words of earlier scanning warps
+                    wpre[0] = 0;
+#pragma unroll
+                    for (int x = 1; x < EQW / 32; ++x) wpre[x] = wpre[x - 1] + sm.wsum[x - 1];
                     for (int p = s0 + tid; p < e0; p += NT) {
                         const int j = (int)sm.cidx[p] - c0;
-                        if (sm.cval[p] != v0 || j < 0 || j >= 32 * kTopkEqWords) continue;
+                        if ((!only && sm.cval[p] != v0) || j < 0 || j >= EQK) continue;
                         const int wd = j >> 5;
-                        const int rank = before + sm.eqpre[wd] + (wd >= 32 ? sm.wsum[0] : 0) +
+                        int off = 0;
+#pragma unroll
+                        for (int x = 1; x < EQW / 32; ++x) off = (wd >> 5) == x ? wpre[x] : off;
+                        const int rank = before + sm.eqpre[wd] + off +
                                          __popc(sm.eqbm[wd] & ((1u << (j & 31)) - 1u));
                         const int pos = bb + gt + rank;
                         if (pos < it.sel) {
@@ -651,7 +665,8 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
                             out_sc[it.base + pos] = topk_from_f<T>(v0);
                         }
                     }
-                    before += sm.wsum[0] + sm.wsum[1];
+#pragma unroll
+                    for (int x = 0; x < EQW / 32; ++x) before += sm.wsum[x];
                     if (tid == 0) sm.neq = 0;
                     named_bar_sync(bar_id, NT);
                 }
