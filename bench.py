@@ -548,6 +548,16 @@ def emit(args, wl, world, ms, ms_max, flops, pairs, value, rows_per_s, e2e_ms, h
     achieved = flops / (ms * 1e-3) / 1e12
     peak = pk["bf16_tflops"]
     traffic = recorded_traffic("score_fwd_kernel<64>/long_fused", SCORE_SRC)
+    clocks = clk.summary()
+    # the tensor pipe's nominal dense bf16 rate at the SM clock sampled during
+    # the timed region: one 128x256x16 MMA (2^20 FLOP) per 128 cycles per SM
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    mhz = clocks.get("sm_mhz")
+    at_clock = None
+    if mhz:
+        pipe = 8192.0 * sms * mhz * 1e6 / 1e12
+        at_clock = {"peak": pipe, "frac": achieved / pipe, "unit": "TFLOP/s",
+                    "basis": f"8192 FLOP/clk/SM x {sms} SMs x {mhz:.0f} MHz (median sampled)"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_max,
@@ -559,12 +569,13 @@ def emit(args, wl, world, ms, ms_max, flops, pairs, value, rows_per_s, e2e_ms, h
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "score_fwd_kernel<64> (fused scoring + top-k)",
                      "peak_source": f"{pk_src} bf16_tflops (burst)",
-                     "algorithmic": f"{pairs} visible pairs x 2*H*D = {flops:.4e} FLOP per launch"},
+                     "algorithmic": f"{pairs} visible pairs x 2*H*D = {flops:.4e} FLOP per launch",
+                     "pipe_at_clock": at_clock},
         "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "pipeline": "copy in / compute / copy out on three streams, two device buffer sets"},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "device_status": status,
     }
     if not args.no_side:
