@@ -81,6 +81,10 @@ struct TopkSmemT {
     static constexpr int kNB = NB;                       // value buckets of an item
     static constexpr int kHist = NB + NB / 32 + 2;       // padded histogram slots
     static constexpr int kEqWords = EQW;                 // bitmap words: 32*EQW keys a chunk
+    // Buckets whose members all hold one score skip the off-score list.  Left
+    // out of the default (fused-kernel) scratch, where the extra code measured
+    // about 1 % slower on normal rows, which never take this path.
+    static constexpr bool kEqOnlyPath = EQW > kTopkEqWords;
     static_assert(EQW % 32 == 0 && EQW >= kTopkSmall && EQW <= 256, "bitmap words");
     static constexpr int kStack = kTopkMaxKeys / CAP + kTopkStackOpt;
     static constexpr int kMed = CAP / (kTopkSmall + 1) + 1;
@@ -565,7 +569,7 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
                 }
                 if (lane == 0) {
                     if (ne <= kTopkSmall) {
-                        sm.med[i] = -1 - b - (ne == 0 ? kEqOnly : 0);
+                        sm.med[i] = -1 - b - ((SM::kEqOnlyPath && ne == 0) ? kEqOnly : 0);
                     } else if (e0 - s0 > kTopkWarpSort) {
                         const int slot = atomicAdd(&sm.nitems, 1);
                         if (slot < kTopkStackOpt) {
@@ -589,8 +593,8 @@ __device__ void topk_item(const T* r, int n, int lo, const TopkItem it, bool cle
             for (int i = 0; i < nmed; ++i) {
                 const int code = sm.med[i];
                 if (code >= 0 || code == INT_MIN) continue;
-                const bool only = -1 - code >= kEqOnly;  // every member holds v0
-                const int b = (-1 - code) & (kEqOnly - 1);
+                const bool only = SM::kEqOnlyPath && -1 - code >= kEqOnly;  // every member holds v0
+                const int b = SM::kEqOnlyPath ? (-1 - code) & (kEqOnly - 1) : -1 - code;
                 const int s0 = bbegin(b) - wbase, e0 = sm.start[hidx(b)] - wbase;
                 const int bb = bbegin(b);  // item-local position of the bucket
                 const float v0 = sm.cval[s0];
