@@ -39,7 +39,7 @@ import workloads  # noqa: E402
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SCORE_SRC = ["sparse_attention_top_tcgen05_gb300/csrc/score_fwd.cuh",
              "sparse_attention_top_tcgen05_gb300/csrc/score_fwd.cu",
-             "sparse_attention_top_tcgen05_gb300/csrc/score_fwd_v4.cu",
+             "sparse_attention_top_tcgen05_gb300/csrc/score_fwd_v4_fused.cu",
              "sparse_attention_top_tcgen05_gb300/csrc/topk.cuh",
              "sparse_attention_top_tcgen05_gb300/csrc/ptx.cuh"]
 

@@ -319,8 +319,8 @@ size_t lidx_workspace_bytes(int op, int64_t B, int64_t S, int64_t Skv, int H, in
 int lidx_device_status(void* stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LIDX_ERR_CUDA;
     // one status word per translation unit with kernels; every one is read (and cleared)
-    const int st[] = {status_score_v4(1), status_score_v4_short(1), status_score_v41(1), status_misc(1),
-                      status_bwd(1)};
+    const int st[] = {status_score_v4(1), status_score_v4_short(1), status_score_v4_fused(1),
+                      status_score_v41(1), status_misc(1), status_bwd(1)};
     int first = 0;
     for (int v : st) {
         if (v < 0) return LIDX_ERR_CUDA;

@@ -58,6 +58,8 @@ cudaError_t score_launch_v4(const ScoreLaunch& a, const CUtensorMap& mq, const C
                             const CUtensorMap& ma, int smem, int grid);
 cudaError_t score_launch_v4_short(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                                   const CUtensorMap& ma, int smem, int grid);
+cudaError_t score_launch_v4_fused(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
+                                  const CUtensorMap& ma, int smem, int grid);
 cudaError_t score_launch_v41(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                              const CUtensorMap& ma, int smem, int grid);
 int score_v41_launch(ScoreLaunch& a);
@@ -114,6 +116,7 @@ int debug_stall();                                    // failure-detection test 
 // per-TU status readers (see LIDX_STATUS_READER): value, or -1 on a CUDA error
 int status_score_v4(int clear);        // status words of the scoring kernels' units
 int status_score_v4_short(int clear);
+int status_score_v4_fused(int clear);
 int status_score_v41(int clear);
 int status_misc(int clear);
 int status_bwd(int clear);

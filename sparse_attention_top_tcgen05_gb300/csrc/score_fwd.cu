@@ -60,9 +60,13 @@ int score_fwd_launch(ScoreLaunch& a) {
     if (p.H < 1 || p.H > 128 || (p.H & (p.H - 1))) return -2;
     CUtensorMap unused;
     memset(&unused, 0, sizeof unused);
-    // rows of at most kTopkShortCap keys: more selection groups with smaller windows
+    // rows of at most kTopkShortCap keys: more selection groups with smaller windows;
+    // else the fused-only configuration when the call asks for nothing more
+    const bool fused_only =
+        p.logits == nullptr && p.idx_in == nullptr && !p.warp_rows && p.act == 0 && p.topk > 0;
     const cudaError_t e = p.Skv <= kTopkShortCap ? score_launch_v4_short(a, mq, mk, unused, smem, grid)
-                                                 : score_launch_v4(a, mq, mk, unused, smem, grid);
+                          : fused_only          ? score_launch_v4_fused(a, mq, mk, unused, smem, grid)
+                                                : score_launch_v4(a, mq, mk, unused, smem, grid);
     a.launched = grid;
     return e == cudaSuccess ? 0 : -1;
 }

@@ -317,13 +317,24 @@ struct RecBuild {
     uint32_t bits[kRecBitTiles / 32];
 };
 
-// SEL (V4 only): the selection runs kTopkGroupsShort groups with a window of
-// kTopkShortCap members, for rows of at most that many keys.
-template <int H, bool V41, bool SEL>
+// Configurations of the V4 kernel (template argument CFG; V4.1 takes kCfgAll):
+//   kCfgAll    three selection groups; every mode of a call (materialised
+//              logits, given indices, per-warp rows, either activation);
+//   kCfgShort  six selection groups with windows of kTopkShortCap members, for
+//              rows of at most that many keys; every mode;
+//   kCfgFused  three groups, fused ReLU scoring and selection only.  Leaving the
+//              other modes out of this instantiation frees registers (no spills
+//              at 72 a thread) and code: the long-context fused forward runs
+//              about 6 % faster than in kCfgAll.
+constexpr int kCfgAll = 0, kCfgShort = 1, kCfgFused = 2;
+
+template <int H, bool V41, int CFG>
 __global__ void __launch_bounds__(kThreads, 1)
     score_fwd_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                      const __grid_constant__ CUtensorMap tma, const ScoreParams p) {
     constexpr int QT = kN / H;
+    constexpr bool SEL = CFG == kCfgShort, FUSED = CFG == kCfgFused;
+    static_assert(!(V41 && CFG != kCfgAll), "V4.1 has one configuration");
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base, formed by pointer arithmetic on the shared array
     // itself so that every access through it stays a shared-memory access
@@ -378,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int swz = p.swz, KB = swz / 2, nkb = p.D / KB;
-    const bool materialise = !V41 && p.logits != nullptr;
+    const bool materialise = !V41 && !FUSED && p.logits != nullptr;
     const bool select = !V41 && p.topk > 0;
 
     if (threadIdx.x == 0) {
@@ -571,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // its weight words per lane, held one unit ahead
         constexpr int CPW = 4 * kN / EW, QW = CPW / H, WPER = H >= 2 ? 2 : 1;
         constexpr int NWL = V41 ? CPW / WPER / 32 : 1;
-        const bool relu = p.act == 0;
+        const bool relu = FUSED || p.act == 0;
         uint32_t wreg[NWL];
 #pragma unroll
         for (int k = 0; k < NWL; ++k)
@@ -962,7 +973,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         static_assert(kTopkBar + NG <= 16, "named barrier ids");
         const int ttid = threadIdx.x - 64 - kEpiThreads;
         const int grp = ttid / GT, gtid = ttid % GT;
-        const bool by_warp = p.warp_rows != 0;
+        const bool by_warp = !FUSED && p.warp_rows != 0;
         const int nsel = by_warp ? kTopkWarps : NG, sel_id = by_warp ? ttid / 32 : grp;
         SMT& sTg = *(SMT*)(smem + L.topk_off + grp * kGroupBytes);
         int i = 0, ucount = -1;
@@ -1006,7 +1017,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     else
                         warp_topk_short<4, false, float>(row + lo, n, lo, p.topk, p.out_idx + orow,
                                                          p.out_sc + orow, lane);
-                } else if (p.idx_in) {
+                } else if (!FUSED && p.idx_in) {
                     row_gather<GT>(row, lo, hi, p.idx_in + orow, p.topk, p.out_idx + orow,
                                                   p.out_sc + orow, gtid, kTopkBar + grp);
                 } else {
@@ -1033,30 +1044,30 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int H, bool V41, bool SEL>
+template <int H, bool V41, int CFG>
 inline cudaError_t launch_h(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                             const CUtensorMap& ma, int smem, int grid) {
-    auto kern = score_fwd_kernel<H, V41, SEL>;
+    auto kern = score_fwd_kernel<H, V41, CFG>;
     cudaError_t e = set_smem_attr((const void*)kern, smem);
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, smem, (cudaStream_t)a.stream>>>(mq, mk, ma, a.p);
     return cudaGetLastError();
 }
 
-// Launches the kernel for the call's head count.  Each (V41, SEL) configuration
+// Launches the kernel for the call's head count.  Each (V41, CFG) configuration
 // is instantiated in a translation unit of its own (score_fwd_*.cu).
-template <bool V41, bool SEL>
+template <bool V41, int CFG>
 inline cudaError_t launch_any(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& ma, int smem, int grid) {
     switch (a.p.H) {
-        case 1: return launch_h<1, V41, SEL>(a, mq, mk, ma, smem, grid);
-        case 2: return launch_h<2, V41, SEL>(a, mq, mk, ma, smem, grid);
-        case 4: return launch_h<4, V41, SEL>(a, mq, mk, ma, smem, grid);
-        case 8: return launch_h<8, V41, SEL>(a, mq, mk, ma, smem, grid);
-        case 16: return launch_h<16, V41, SEL>(a, mq, mk, ma, smem, grid);
-        case 32: return launch_h<32, V41, SEL>(a, mq, mk, ma, smem, grid);
-        case 64: return launch_h<64, V41, SEL>(a, mq, mk, ma, smem, grid);
-        case 128: return launch_h<128, V41, SEL>(a, mq, mk, ma, smem, grid);
+        case 1: return launch_h<1, V41, CFG>(a, mq, mk, ma, smem, grid);
+        case 2: return launch_h<2, V41, CFG>(a, mq, mk, ma, smem, grid);
+        case 4: return launch_h<4, V41, CFG>(a, mq, mk, ma, smem, grid);
+        case 8: return launch_h<8, V41, CFG>(a, mq, mk, ma, smem, grid);
+        case 16: return launch_h<16, V41, CFG>(a, mq, mk, ma, smem, grid);
+        case 32: return launch_h<32, V41, CFG>(a, mq, mk, ma, smem, grid);
+        case 64: return launch_h<64, V41, CFG>(a, mq, mk, ma, smem, grid);
+        case 128: return launch_h<128, V41, CFG>(a, mq, mk, ma, smem, grid);
         default: return cudaErrorInvalidValue;
     }
 }

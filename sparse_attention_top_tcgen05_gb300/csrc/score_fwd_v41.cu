@@ -8,7 +8,7 @@ LIDX_STATUS_READER(status_score_v41)
 
 cudaError_t score_launch_v41(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& ma, int smem, int grid) {
-    return launch_any<true, false>(a, mq, mk, ma, smem, grid);
+    return launch_any<true, kCfgAll>(a, mq, mk, ma, smem, grid);
 }
 
 }  // namespace lidx

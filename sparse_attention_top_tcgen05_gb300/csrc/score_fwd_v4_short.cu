@@ -8,7 +8,7 @@ LIDX_STATUS_READER(status_score_v4_short)
 
 cudaError_t score_launch_v4_short(const ScoreLaunch& a, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& ma, int smem, int grid) {
-    return launch_any<false, true>(a, mq, mk, ma, smem, grid);
+    return launch_any<false, kCfgShort>(a, mq, mk, ma, smem, grid);
 }
 
 }  // namespace lidx
