@@ -223,11 +223,13 @@ WORKLOAD_DESC = {
 
 def config_of(wl, n):
     desc = WORKLOAD_DESC.get(wl.name, "V4 fused score+causal mask+top-k")
+    q_mb = wl.B * wl.S * wl.H * wl.D * 2 / 1e6
     return {"workload": f"{wl.name}: {desc}",
             "B": wl.B, "S": wl.S, "H": wl.H, "D": wl.D, "Skv": wl.Skv,
             "compress_ratio": wl.ratio, "topk": wl.topk, "act": "relu",
             "inputs": "bf16 q,k ~N(0,1/D); fp32 w ~N(0,1/H); seed 0",
-            "l2": "inputs larger than L2 (q = 537 MB > 129 MB), no flush",
+            "l2": (f"inputs larger than L2 (q = {q_mb:.0f} MB > 129 MB), no flush" if q_mb > 129
+                   else f"q = {q_mb:.0f} MB fits in L2 (129 MB): a profiling size, not the workload"),
             "parallelism": f"replicas x{n}"}
 
 

@@ -377,7 +377,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
                     if (!(ok = mbar_wait(r_free + r, ((tcount / kBRegions) & 1) ^ 1, p.wait_ns))) break;
                     tc_fence_after();
                     const uint32_t d = tmem_base + r * kBT;
-                    const uint64_t a0 = ub == 2 ? rd[2] : (ub == 1 ? rd[1] : rd[0]);
+                    uint64_t a0 = rd[0];
+#pragma unroll
+                    for (int j = 1; j < kBRes; ++j) a0 = ub == j ? rd[j] : a0;
                     uint64_t b0 = sd[0];
 #pragma unroll
                     for (int j = 1; j < kBStages; ++j) b0 = st == j ? sd[j] : b0;
@@ -391,13 +393,20 @@ __global__ void __launch_bounds__(kBThreads, 1)
                         for (int j = 1; j < kBLookahead; ++j) queue[j - 1] = queue[j];
                         --nq;
                     }
-                    queue[nq++] = Pend{r, st, ub, tcount, uc, idx == 0, idx == n - 1};
+                    // constant indices keep the queue in registers
+                    const Pend pend{r, st, ub, tcount, uc, idx == 0, idx == n - 1};
+#pragma unroll
+                    for (int j = 0; j < kBLookahead; ++j)
+                        if (j == nq) queue[j] = pend;
+                    ++nq;
                     ++kcount;
                     ++tcount;
                     ++idx;
                 }
             }
-            for (int j = 0; ok && j < nq; ++j) ok = second(queue[j]);
+#pragma unroll
+            for (int j = 0; j < kBLookahead; ++j)
+                if (ok && j < nq) ok = second(queue[j]);
         }
     } else {
         // --------------------------------------------------------- epilogue
@@ -549,8 +558,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
                             for (int v = 0; v < 8; ++v)
                                 reinterpret_cast<float4*>(dst)[v] =
                                     make_float4(out[4 * v], out[4 * v + 1], out[4 * v + 2], out[4 * v + 3]);
-                        } else {
-                            for (int v = 0; v < dn; ++v) dst[v] = out[v];
+                        } else {  // ragged last chunk; constant indices keep `out` in registers
+#pragma unroll
+                            for (int v = 0; v < 32; ++v)
+                                if (v < dn) dst[v] = out[v];
                         }
                     } else {
                         uint16_t* dst = (uint16_t*)p.dq + o;
@@ -563,8 +574,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
                                 reinterpret_cast<uint4*>(dst)[v] =
                                     make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
                         } else {
-                            for (int v = 0; v < dn; ++v)
-                                dst[v] = (uint16_t)(bf16x2_rn(out[v], 0.f) & 0xffffu);
+#pragma unroll
+                            for (int v = 0; v < 32; ++v)
+                                if (v < dn) dst[v] = (uint16_t)(bf16x2_rn(out[v], 0.f) & 0xffffu);
                         }
                     }
                 }
