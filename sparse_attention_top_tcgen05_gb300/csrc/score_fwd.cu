@@ -61,12 +61,14 @@ int score_fwd_launch(ScoreLaunch& a) {
     CUtensorMap unused;
     memset(&unused, 0, sizeof unused);
     // rows of at most kTopkShortCap keys: more selection groups with smaller windows;
-    // else the fused-only configuration when the call asks for nothing more
-    const bool fused_only =
-        p.logits == nullptr && p.idx_in == nullptr && !p.warp_rows && p.act == 0 && p.topk > 0;
-    const cudaError_t e = p.Skv <= kTopkShortCap ? score_launch_v4_short(a, mq, mk, unused, smem, grid)
-                          : fused_only          ? score_launch_v4_fused(a, mq, mk, unused, smem, grid)
-                                                : score_launch_v4(a, mq, mk, unused, smem, grid);
+    // the fused-only configuration when the call asks for nothing more; else the
+    // general one
+    const bool plain = p.idx_in == nullptr && !p.warp_rows && p.act == 0;
+    const bool short_rows = plain && p.Skv <= kTopkShortCap;
+    const bool fused_only = plain && p.logits == nullptr && p.topk > 0;
+    const cudaError_t e = short_rows   ? score_launch_v4_short(a, mq, mk, unused, smem, grid)
+                          : fused_only ? score_launch_v4_fused(a, mq, mk, unused, smem, grid)
+                                       : score_launch_v4(a, mq, mk, unused, smem, grid);
     a.launched = grid;
     return e == cudaSuccess ? 0 : -1;
 }
