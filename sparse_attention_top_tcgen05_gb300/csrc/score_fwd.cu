@@ -65,7 +65,7 @@ int score_fwd_launch(ScoreLaunch& a) {
     // general one
     const bool plain = p.idx_in == nullptr && !p.warp_rows && p.act == 0;
     const bool short_rows = plain && p.Skv <= kTopkShortCap;
-    const bool fused_only = plain && p.logits == nullptr && p.topk > 0;
+    const bool fused_only = plain && p.logits == nullptr && p.topk > 0 && p.D == 128;
     const cudaError_t e = short_rows   ? score_launch_v4_short(a, mq, mk, unused, smem, grid)
                           : fused_only ? score_launch_v4_fused(a, mq, mk, unused, smem, grid)
                                        : score_launch_v4(a, mq, mk, unused, smem, grid);

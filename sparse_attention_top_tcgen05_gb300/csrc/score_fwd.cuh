@@ -324,10 +324,11 @@ struct RecBuild {
 //              rows of at most that many keys; ReLU, fused or materialised logits,
 //              no given indices or per-warp rows (7 % faster on the C4 layer than
 //              with them);
-//   kCfgFused  three groups, fused ReLU scoring and selection only.  Leaving the
-//              other modes out of this instantiation frees registers (no spills
-//              at 72 a thread) and code: the long-context fused forward runs
-//              about 6 % faster than in kCfgAll.
+//   kCfgFused  three groups, fused ReLU scoring and selection only, D = 128.
+//              Leaving the other modes out of this instantiation frees registers
+//              (no spills at 72 a thread) and code, and a constant D makes the
+//              shared-memory layout constant: the long-context fused forward runs
+//              about 9 % faster than in kCfgAll.
 constexpr int kCfgAll = 0, kCfgShort = 1, kCfgFused = 2;
 
 template <int H, bool V41, int CFG>
@@ -341,7 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte aligned base, formed by pointer arithmetic on the shared array
     // itself so that every access through it stays a shared-memory access
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const SmemLayout L = smem_layout(p.D);
+    // the fused-only configuration takes D = 128: its layout is constant
+    const int D = FUSED ? 128 : p.D;
+    const SmemLayout L = smem_layout(D);
     uint8_t* sQ = smem + L.q_off;
     uint8_t* sK = smem + L.k_off;
     float* sW = (float*)(smem + L.w_off);
@@ -369,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   "second query tile, visibility ring, weights and records exceed the scratch");
     const bool vis_tma = VIS_RING && p.vis_tma;
     uint8_t* const sQ1 = smem + L.topk_off;  // second query tile (V4.1 only)
-    uint8_t* const sVis = sQ1 + kN * p.D * 2;
+    uint8_t* const sVis = sQ1 + kN * D * 2;
     uint32_t* const sWw = reinterpret_cast<uint32_t*>(sVis + kVisStages * 32 * kM);  // [EW][64]
     int4* const sRec = reinterpret_cast<int4*>(sWw + 16 * 64);                        // [kRecSlots]
     RecBuild* const sBuild = reinterpret_cast<RecBuild*>(sRec + kRecSlots);           // [2]
@@ -390,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = (uint32_t*)(smem + L.tmem_off);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int swz = p.swz, KB = swz / 2, nkb = p.D / KB;
+    const int swz = FUSED ? 128 : p.swz, KB = swz / 2, nkb = D / KB;
     const bool materialise = !V41 && !FUSED && p.logits != nullptr;
     const bool select = !V41 && p.topk > 0;
 
@@ -461,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int qb = qcount % NQB;
                 if (!(ok = mbar_wait(q_emptyv(qb), ((qcount / NQB) & 1) ^ 1, p.wait_ns))) break;
                 ++qcount;
-                mbar_arrive_expect_tx(q_fullv(qb), kN * p.D * 2);
+                mbar_arrive_expect_tx(q_fullv(qb), kN * D * 2);
                 for (int kb = 0; kb < nkb; ++kb)
                 {
                     if constexpr (V41)  // q [B,S,H,D]: dims (D, H, S, B)
@@ -485,8 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!tile_active<V41>(p, un, kt)) continue;
                     const int kc = kcount++, st = kc % kStages;
                     if (!(ok = mbar_wait(k_empty + st, ((kc / kStages) & 1) ^ 1, p.wait_ns))) break;
-                    uint8_t* dst = sK + st * kM * p.D * 2;
-                    mbar_arrive_expect_tx(k_full + st, kM * p.D * 2);
+                    uint8_t* dst = sK + st * kM * D * 2;
+                    mbar_arrive_expect_tx(k_full + st, kM * D * 2);
                     for (int kb = 0; kb < nkb; ++kb) {
                         if constexpr (V41)  // k [B,Skv,D]: dims (D, Skv, B)
                             tma_load_3d(dst + kb * kM * swz, &tmk, k_full + st, kb * KB, kt * kM, un.b);
@@ -508,10 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_bf16_f32(kM, kN);
             // Every descriptor the tile loop needs is built once per CTA, exactly as
             // the per-step formula builds it (address + offset, then masked).
-            const int nk = p.D / 16;
+            const int nk = D / 16;
             uint64_t ad[kStages][8], bd[8];
             {
-                const uint32_t a0 = smem_u32(sK), stage = (uint32_t)(kM * p.D * 2), b0 = smem_u32(sQ);
+                const uint32_t a0 = smem_u32(sK), stage = (uint32_t)(kM * D * 2), b0 = smem_u32(sQ);
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const int kb = (k * 16) / KB, koff = ((k * 16) % KB) * 2;
