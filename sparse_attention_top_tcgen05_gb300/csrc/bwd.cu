@@ -12,7 +12,7 @@
 // Four launches, all on the caller's stream:
 //   1. bwd_scatter_kernel: the selected grads become a dense G[b,s,t] (0 where
 //      nothing is selected; slots outside the row's range are dropped).
-//   2. bwd_tile_kernel<H, 0>, query-major.  A persistent CTA takes tiles of
+//   2. bwd_tile_kernel<H, 0, D128>, query-major.  A persistent CTA takes tiles of
 //      128 (query, head) rows and sweeps their visible keys 128 at a time:
 //        X = Q K^T                 tcgen05, bf16 -> fp32 into TMEM
 //        P = G w act'(X), dw += G act(X)   epilogue warps, one TMEM lane each;
@@ -20,7 +20,7 @@
 //        dq += P_hi K + P_lo K     tcgen05 with A read from TMEM, K as an
 //                                  MN-major operand of the same shared tile
 //      dq and dw are written once per row tile.
-//   3. bwd_tile_kernel<H, 1>, key-major: the same pipeline with the roles of
+//   3. bwd_tile_kernel<H, 1, D128>, key-major: the same pipeline with the roles of
 //      the operands swapped -- a tile of 128 keys sweeps a chunk of query tiles
 //      (128 (query, head) columns each), X^T = K Q^T, P^T, dk += P^T Q -- and
 //      writes one partial dk per (key tile, chunk).
@@ -192,7 +192,8 @@ __device__ __forceinline__ void split_hi_lo(const float (&P)[32], uint32_t (&hi)
     }
 }
 
-template <int H, int MODE>
+// D128: D = 128, so that the shared-memory layout and the column loops are constant
+template <int H, int MODE, bool D128>
 __global__ void __launch_bounds__(kBThreads, 1)
     bwd_tile_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
                     const __grid_constant__ CUtensorMap tmg, const __grid_constant__ CUtensorMap tmw,
@@ -205,7 +206,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
     constexpr uint32_t kWBytes = (kStaged && MODE == 1) ? QT * H * 4 : 0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const int nkb = p.nkb;
+    const int nkb = D128 ? 2 : p.nkb;
+    const int Dp = D128 ? 128 : p.Dp, D = D128 ? 128 : p.D;
     const uint32_t tile_bytes = kBTileBytes * nkb;
     const uint32_t stage_bytes = tile_bytes + (kGBytes + kWBytes + 1023u) / 1024u * 1024u;
     uint8_t* sRes = smem;                          // [kBRes] resident tiles
@@ -313,8 +315,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
         // ------------------------------------------------------- MMA issuer
         if (lane == 0) {
             const uint32_t idesc_x = idesc_bf16_f32(kBT, kBT);
-            const uint32_t idesc_2 = idesc_bf16_f32(kBT, (uint32_t)p.Dp) | (1u << 16);  // B MN-major
-            const int nk = p.Dp / 16;
+            const uint32_t idesc_2 = idesc_bf16_f32(kBT, (uint32_t)Dp) | (1u << 16);  // B MN-major
+            const int nk = Dp / 16;
             // base descriptors of every buffer; a k-step adds its byte offset / 16 to the
             // 14-bit start-address field (shared addresses stay below 256 KB: no carry)
             uint64_t rd[kBRes], sd[kBStages], md[kBStages];
@@ -536,7 +538,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
 #pragma unroll 1
             for (int c = 2 * chalf; c < 2 * chalf + 2; ++c) {
             float out[32];
-            if (n > 0 && 32 * c < p.Dp) {
+            if (n > 0 && 32 * c < Dp) {
                 uint32_t ar[32];
                 tmem_ld32(lane_addr + acc_col + 32 * c, ar);
                 tmem_ld_wait();
@@ -547,10 +549,10 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 for (int v = 0; v < 32; ++v) out[v] = 0.f;
             }
             const int d0 = 32 * c;
-            const int dn = min(32, p.D - d0);  // valid output columns of this chunk
+            const int dn = min(32, D - d0);  // valid output columns of this chunk
             if constexpr (MODE == 0) {
                 if (rvalid && dn > 0) {
-                    const size_t o = (((size_t)s * p.B + un.b) * H + h) * p.D + d0;
+                    const size_t o = (((size_t)s * p.B + un.b) * H + h) * D + d0;
                     if (p.grad_dtype == 0) {
                         float* dst = (float*)p.dq + o;
                         if (dn == 32) {
@@ -581,8 +583,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
                     }
                 }
             } else {
-                if (dn > 0 && d0 < p.Dp) {
-                    float* dst = p.part + ((size_t)u * kBT + row) * p.Dp + d0;
+                if (dn > 0 && d0 < Dp) {
+                    float* dst = p.part + ((size_t)u * kBT + row) * Dp + d0;
 #pragma unroll
                     for (int v = 0; v < 8; ++v)
                         reinterpret_cast<float4*>(dst)[v] =
@@ -820,15 +822,15 @@ static size_t bwd_smem_bytes(int nkb, int H, int MODE) {
     return 1024 + kBRes * tile + kBStages * (tile + extra) + 2 * 4 * kBT * 4 + 32 * 8 + 16;
 }
 
-template <int H>
-static cudaError_t bwd_tiles_h(const CUtensorMap* maps, const BwdParams& p0, const BwdLaunch& a) {
+template <int H, bool D128>
+static cudaError_t bwd_tiles_hd(const CUtensorMap* maps, const BwdParams& p0, const BwdLaunch& a) {
     BwdParams p = p0;
     // dq and dw, query-major; at least 120 KB of shared memory so that one CTA
     // (and its 512 TMEM columns) owns each SM
     {
         int smem = (int)bwd_smem_bytes(p.nkb, H, 0);
         if (smem < 120 * 1024) smem = 120 * 1024;
-        auto kern = bwd_tile_kernel<H, 0>;
+        auto kern = bwd_tile_kernel<H, 0, D128>;
         cudaError_t e = set_smem_attr((const void*)kern, smem);
         if (e != cudaSuccess) return e;
         p.num_units = p.B * p.qtiles;
@@ -841,7 +843,7 @@ static cudaError_t bwd_tiles_h(const CUtensorMap* maps, const BwdParams& p0, con
     {
         int smem = (int)bwd_smem_bytes(p.nkb, H, 1);
         if (smem < 120 * 1024) smem = 120 * 1024;
-        auto kern = bwd_tile_kernel<H, 1>;
+        auto kern = bwd_tile_kernel<H, 1, D128>;
         cudaError_t e = set_smem_attr((const void*)kern, smem);
         if (e != cudaSuccess) return e;
         p.num_units = p.B * p.U;
@@ -849,6 +851,11 @@ static cudaError_t bwd_tiles_h(const CUtensorMap* maps, const BwdParams& p0, con
         if (grid > 0) kern<<<grid, kBThreads, smem, a.stream>>>(maps[0], maps[1], maps[2], maps[3], p);
         return cudaGetLastError();
     }
+}
+
+template <int H>
+static cudaError_t bwd_tiles_h(const CUtensorMap* maps, const BwdParams& p, const BwdLaunch& a) {
+    return p.D == 128 ? bwd_tiles_hd<H, true>(maps, p, a) : bwd_tiles_hd<H, false>(maps, p, a);
 }
 
 cudaError_t bwd_launch(const BwdLaunch& a) {
