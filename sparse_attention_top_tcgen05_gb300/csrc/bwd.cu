@@ -192,7 +192,8 @@ __device__ __forceinline__ void split_hi_lo(const float (&P)[32], uint32_t (&hi)
     }
 }
 
-// D128: D = 128, so that the shared-memory layout and the column loops are constant
+// D128: D = 128 and ReLU, so that the shared-memory layout, the column loops and
+// the activation are constant (other calls take D128 = false)
 template <int H, int MODE, bool D128>
 __global__ void __launch_bounds__(kBThreads, 1)
     bwd_tile_kernel(const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmk,
@@ -478,7 +479,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
 #pragma unroll
                         for (int v = 0; v < 32; ++v) {
                             const float xv = __uint_as_float(xr[v]);
-                            if (p.act == 0) {
+                            if (D128 || p.act == 0) {
                                 dw4[v & 3] = fmaf(g[v], fmaxf(xv, 0.f), dw4[v & 3]);
                                 P[v] = xv > 0.f ? g[v] * wv : 0.f;
                             } else {
@@ -514,7 +515,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
 #pragma unroll
                         for (int v = 0; v < 32; ++v) {
                             const float xv = __uint_as_float(xr[v]);
-                            P[v] = (p.act == 0) ? (xv > 0.f ? gw[v] : 0.f) : gw[v];
+                            P[v] = (D128 || p.act == 0) ? (xv > 0.f ? gw[v] : 0.f) : gw[v];
                         }
                     }
                     uint32_t hi[16], lo[16];
@@ -855,7 +856,8 @@ static cudaError_t bwd_tiles_hd(const CUtensorMap* maps, const BwdParams& p0, co
 
 template <int H>
 static cudaError_t bwd_tiles_h(const CUtensorMap* maps, const BwdParams& p, const BwdLaunch& a) {
-    return p.D == 128 ? bwd_tiles_hd<H, true>(maps, p, a) : bwd_tiles_hd<H, false>(maps, p, a);
+    const bool d128 = p.D == 128 && p.act == 0;
+    return d128 ? bwd_tiles_hd<H, true>(maps, p, a) : bwd_tiles_hd<H, false>(maps, p, a);
 }
 
 cudaError_t bwd_launch(const BwdLaunch& a) {
