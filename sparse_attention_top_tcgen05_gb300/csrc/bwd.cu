@@ -336,7 +336,8 @@ __global__ void __launch_bounds__(kBThreads, 1)
                 bool first, last;
             };
             bool ok = true;
-            auto second = [&](const Pend& t) -> bool {
+            // by value: a reference kept the queue in local memory
+            auto second = [&](const Pend t) -> bool {
                 if (!mbar_wait(p_full + t.r, (t.tc / kBRegions) & 1, p.wait_ns)) return false;
                 if (t.first && !mbar_wait(acc_empty, (t.uc & 1) ^ 1, p.wait_ns)) return false;
                 tc_fence_after();
