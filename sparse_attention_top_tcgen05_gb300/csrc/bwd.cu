@@ -180,14 +180,35 @@ __device__ __forceinline__ uint32_t bf16x2_rn(float lo_elem, float hi_elem) {
     return r;
 }
 
+// Packed fp32 pairs: each lane of the pair rounded as the scalar operation rounds.
+__device__ __forceinline__ void sub2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "sub.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void mul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mul.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "mov.b64 d, {%0, %1};\n\tfma.rn.f32x2 d, a, b, d;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // P of 32 columns -> packed bf16 hi and lo halves (element 2c in the low half).
+// P - hi is exact in fp32, so lo carries the next 8 bits of P.
 __device__ __forceinline__ void split_hi_lo(const float (&P)[32], uint32_t (&hi)[16], uint32_t (&lo)[16]) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
         const uint32_t h2 = bf16x2_rn(P[2 * c], P[2 * c + 1]);
         hi[c] = h2;
-        const float r0 = P[2 * c] - __uint_as_float(h2 << 16);
-        const float r1 = P[2 * c + 1] - __uint_as_float(h2 & 0xffff0000u);
+        float r0, r1;
+        sub2(r0, r1, P[2 * c], P[2 * c + 1], __uint_as_float(h2 << 16), __uint_as_float(h2 & 0xffff0000u));
         lo[c] = bf16x2_rn(r0, r1);
     }
 }
@@ -478,15 +499,15 @@ __global__ void __launch_bounds__(kBThreads, 1)
                         }
                         tmem_ld_wait();
 #pragma unroll
-                        for (int v = 0; v < 32; ++v) {
-                            const float xv = __uint_as_float(xr[v]);
-                            if (D128 || p.act == 0) {
-                                dw4[v & 3] = fmaf(g[v], fmaxf(xv, 0.f), dw4[v & 3]);
-                                P[v] = xv > 0.f ? g[v] * wv : 0.f;
-                            } else {
-                                dw4[v & 3] = fmaf(g[v], xv, dw4[v & 3]);
-                                P[v] = g[v] * wv;
-                            }
+                        for (int v = 0; v < 32; v += 2) {
+                            const float x0 = __uint_as_float(xr[v]), x1 = __uint_as_float(xr[v + 1]);
+                            const bool relu = D128 || p.act == 0;
+                            const float a0 = relu ? fmaxf(x0, 0.f) : x0, a1 = relu ? fmaxf(x1, 0.f) : x1;
+                            fma2(dw4[v & 3], dw4[(v & 3) + 1], g[v], g[v + 1], a0, a1);
+                            float p0, p1;
+                            mul2(p0, p1, g[v], g[v + 1], wv, wv);
+                            P[v] = (!relu || x0 > 0.f) ? p0 : 0.f;
+                            P[v + 1] = (!relu || x1 > 0.f) ? p1 : 0.f;
                         }
                     } else {
                         // columns = (query, head) 32c + i of query tile x; this thread's key t
@@ -499,8 +520,9 @@ __global__ void __launch_bounds__(kBThreads, 1)
                                 const float4 w4 = *reinterpret_cast<const float4*>(wS + 32 * c + v);
                                 const float wv4[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                                for (int e = 0; e < 4; ++e)
-                                    gw[v + e] = gS[((32 * c + v + e) / H) * kBT + row] * wv4[e];
+                                for (int e = 0; e < 4; e += 2)
+                                    mul2(gw[v + e], gw[v + e + 1], gS[((32 * c + v + e) / H) * kBT + row],
+                                         gS[((32 * c + v + e + 1) / H) * kBT + row], wv4[e], wv4[e + 1]);
                             }
                         } else {
 #pragma unroll
