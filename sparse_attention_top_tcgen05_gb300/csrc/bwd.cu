@@ -471,7 +471,7 @@ __global__ void __launch_bounds__(kBThreads, 1)
                     const int tc = tcount++;
                     if (!(ok = mbar_wait(x_full + r, (tc / kBRegions) & 1, p.wait_ns))) break;
                     tc_fence_after();
-#pragma unroll 1
+#pragma unroll
                     for (int cc = 2 * chalf; cc < 2 * chalf + 2; ++cc) {
                     const int c = cc;
                     uint32_t xr[32];
