@@ -310,9 +310,29 @@ def side_workloads(lidx, pk, names=None):
             fn()
         torch.cuda.synchronize()
         host_us = (time.perf_counter() - t0) / 200 * 1e6
+        # device time of one call: 20 calls captured in a CUDA graph and replayed, so
+        # that host launch latency is out of the measurement
+        dev_us = None
+        try:
+            g = torch.cuda.CUDAGraph()
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                fn()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=side):
+                    for _ in range(20):
+                        fn()
+            torch.cuda.synchronize()
+            for _ in range(3):
+                g.replay()
+            dev_us = 1e3 * time_steps(g.replay, 50, torch.cuda.current_stream()) / 20
+        except RuntimeError as e:  # capture refused: report the back-to-back rate only
+            dev_us = f"unavailable: {e}"
         out["tiny"] = {"us_per_call": 1e3 * time_steps(fn, 200, stream), "host_us_per_call": host_us,
-                       "launches": 1, "note": "back-to-back calls, L2 warm; host_us includes the "
-                       "Python binding and the C ABI's argument checks"}
+                       "device_us_per_call": dev_us, "launches": 1,
+                       "note": "back-to-back calls, L2 warm; host_us includes the Python binding and "
+                       "the C ABI's argument checks; device_us from a CUDA-graph replay of 20 calls"}
         del q, k, w, idx, sc, lg
 
     def _c4_fwd():
