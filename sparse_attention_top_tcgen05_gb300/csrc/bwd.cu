@@ -24,7 +24,7 @@
 //      the operands swapped -- a tile of 128 keys sweeps a chunk of query tiles
 //      (128 (query, head) columns each), X^T = K Q^T, P^T, dk += P^T Q -- and
 //      writes one partial dk per (key tile, chunk).
-//   4. bwd_reduce_kernel: dk = each key tile's partials summed in chunk order.
+//   4. bwd_reduce_kernel: dk = each key tile's partials summed in a fixed order.
 // No atomic operation touches dq, dk or dw: the results are deterministic.
 //
 // P is split into two bf16 halves (hi = bf16(P), lo = bf16(P - hi)) because the
@@ -709,36 +709,64 @@ __host__ __device__ __forceinline__ int bwd_c0(bool causal, int kt, int ratio, i
 }
 
 // dk[t,b,:] = sum over the chunks c of key tile t/128 of part[unit(b, c, t/128)][t%128][:],
-// in chunk order.
-__global__ void bwd_reduce_kernel(const float* __restrict__ part, int B, int Skv, int D, int Dp, int U,
-                                  const __grid_constant__ ChunkTable tab, int nchunks, int CH, int QT,
-                                  int qtiles, int ratio, int causal, int grad_dtype, void* dk) {
+// in a fixed order: the chunk range is cut into kReduceSplit runs, each summed in chunk
+// order by its own thread, and the run sums are added pairwise ((r0 + r1) + (r2 + r3)).
+// A block takes kReduceOut outputs (4 columns each) at a time, so that enough loads are
+// in flight for a sum over only tens of chunks.
+constexpr int kReduceSplit = 4, kReduceOut = 64, kReduceThreads = kReduceSplit * kReduceOut;
+
+__global__ void __launch_bounds__(kReduceThreads)
+    bwd_reduce_kernel(const float* __restrict__ part, int B, int Skv, int D, int Dp, int U,
+                      const __grid_constant__ ChunkTable tab, int nchunks, int CH, int QT, int qtiles,
+                      int ratio, int causal, int grad_dtype, void* dk) {
+    __shared__ float4 runs[kReduceSplit][kReduceOut];
     const int D4 = D / 4;
     const int64_t n = (int64_t)B * Skv * D4;
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n;
-         e += (int64_t)gridDim.x * blockDim.x) {
-        const int d4 = (int)(e % D4) * 4;
-        const int64_t bt = e / D4;
-        const int t = (int)(bt % Skv), b = (int)(bt / Skv);
-        const int kt = t / kBT, tl = t % kBT;
+    const int64_t ngroups = (n + kReduceOut - 1) / kReduceOut;
+    const int o_local = threadIdx.x % kReduceOut, q = threadIdx.x / kReduceOut;
+    for (int64_t g = blockIdx.x; g < ngroups; g += gridDim.x) {
+        const int64_t e = g * kReduceOut + o_local;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        // one accumulator in chunk order; the unrolling only keeps loads in flight
-#pragma unroll 8
-        for (int c = bwd_c0(causal != 0, kt, ratio, QT, qtiles, CH, nchunks); c < nchunks; ++c) {
-            const int u = b * U + tab.cpre[c] + kt;
-            const float4 v = *reinterpret_cast<const float4*>(part + ((size_t)u * kBT + tl) * Dp + d4);
-            acc.x += v.x;
-            acc.y += v.y;
-            acc.z += v.z;
-            acc.w += v.w;
+        int t = 0, b = 0, d4 = 0;
+        if (e < n) {
+            d4 = (int)(e % D4) * 4;
+            const int64_t bt = e / D4;
+            t = (int)(bt % Skv);
+            b = (int)(bt / Skv);
+            const int kt = t / kBT, tl = t % kBT;
+            const int c0 = bwd_c0(causal != 0, kt, ratio, QT, qtiles, CH, nchunks), len = nchunks - c0;
+            const int ca = c0 + (int)((int64_t)len * q / kReduceSplit);
+            const int cb = c0 + (int)((int64_t)len * (q + 1) / kReduceSplit);
+            // one accumulator in chunk order; the unrolling only keeps loads in flight
+#pragma unroll 4
+            for (int c = ca; c < cb; ++c) {
+                const int u = b * U + tab.cpre[c] + kt;
+                const float4 v = *reinterpret_cast<const float4*>(part + ((size_t)u * kBT + tl) * Dp + d4);
+                acc.x += v.x;
+                acc.y += v.y;
+                acc.z += v.z;
+                acc.w += v.w;
+            }
         }
-        const size_t o = ((size_t)t * B + b) * D + d4;
-        if (grad_dtype == 0) {
-            *reinterpret_cast<float4*>((float*)dk + o) = acc;
-        } else {
-            const uint32_t lo = bf16x2_rn(acc.x, acc.y), hi = bf16x2_rn(acc.z, acc.w);
-            *reinterpret_cast<uint2*>((uint16_t*)dk + o) = make_uint2(lo, hi);
+        runs[q][o_local] = acc;
+        __syncthreads();
+        if (q == 0 && e < n) {
+            const float4 r1 = runs[1][o_local], r2 = runs[2][o_local], r3 = runs[3][o_local];
+            static_assert(kReduceSplit == 4, "pairwise combination of four runs");
+            float4 sum;
+            sum.x = (acc.x + r1.x) + (r2.x + r3.x);
+            sum.y = (acc.y + r1.y) + (r2.y + r3.y);
+            sum.z = (acc.z + r1.z) + (r2.z + r3.z);
+            sum.w = (acc.w + r1.w) + (r2.w + r3.w);
+            const size_t o = ((size_t)t * B + b) * D + d4;
+            if (grad_dtype == 0) {
+                *reinterpret_cast<float4*>((float*)dk + o) = sum;
+            } else {
+                const uint32_t lo = bf16x2_rn(sum.x, sum.y), hi = bf16x2_rn(sum.z, sum.w);
+                *reinterpret_cast<uint2*>((uint16_t*)dk + o) = make_uint2(lo, hi);
+            }
         }
+        __syncthreads();  // runs[] is reused by the next group
     }
 }
 
@@ -969,9 +997,9 @@ cudaError_t bwd_launch(const BwdLaunch& a) {
     ChunkTable tab;
     memcpy(tab.cpre, pl.cpre, sizeof(int) * (pl.nchunks + 1));
     const int64_t n = (int64_t)a.B * a.Skv * (a.D / 4);
-    int64_t grid = (n + 255) / 256;
+    int64_t grid = (n + kReduceOut - 1) / kReduceOut;
     if (grid > (int64_t)a.num_sms * 8) grid = (int64_t)a.num_sms * 8;
-    bwd_reduce_kernel<<<(unsigned)grid, 256, 0, a.stream>>>(part, a.B, a.Skv, a.D, pl.Dp, pl.U, tab,
+    bwd_reduce_kernel<<<(unsigned)grid, kReduceThreads, 0, a.stream>>>(part, a.B, a.Skv, a.D, pl.Dp, pl.U, tab,
                                                            pl.nchunks, pl.CH, pl.QT, pl.qtiles, a.ratio,
                                                            a.ks == nullptr ? 1 : 0, a.grad_dtype, a.dk);
     return cudaGetLastError();
