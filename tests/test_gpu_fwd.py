@@ -249,6 +249,22 @@ def test_given_indices_score_only_those_pairs(H, D, B, S, Skv, ratio, topk):
         assert_scores_close(osc.cpu().numpy().reshape(B * S, topk), ref, "given-index scores")
 
 
+@pytest.mark.parametrize("B,S,Skv,ratio,topk", [(1, 5000, 1250, 4, 512), (2, 2100, 1100, 1, 1024)])
+def test_fused_only_configuration(B, S, Skv, ratio, topk):
+    """D = 128, ReLU, Skv > 1024 and no logits: the fused call runs the fused-only
+    build, the materialised one the general build.  Both compute the same fp32
+    scores, so their results are identical, and they equal the oracle."""
+    g = np.random.default_rng(S + Skv)
+    H, D = 64, 128
+    q = workloads.to_bf16(g.standard_normal((S, B, H, D)).astype(np.float32) / np.sqrt(D))
+    k = workloads.to_bf16(g.standard_normal((Skv, B, D)).astype(np.float32) / np.sqrt(D))
+    w = torch.from_numpy((g.standard_normal((S, B, H)) / np.sqrt(H)).astype(np.float32))
+    rows = np.concatenate([np.arange(0, B * S, 37), [S - 1, B * S - 1]])  # the oracle on a sample
+    i1, s1, _ = full_check(q, k, w, ratio, topk, materialise=True, rows=rows)
+    i2, s2, _ = run_fwd(q, k, w, ratio, topk, False)
+    assert np.array_equal(i1, i2) and np.array_equal(s1, s2)
+
+
 def test_fused_forward_beyond_one_selection_window():
     """Rows with more visible keys than one shared-memory window of candidates
     (Skv 9000, ratio 1): the fused and materialised paths agree, the selection
