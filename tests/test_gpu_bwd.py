@@ -62,6 +62,7 @@ def selection(B, S, Skv, ratio, topk, seed):
     (1, 200, 16, 64, 300, 2, 50),     # heads below 32: one grad per column in the key-major pass
     (2, 150, 32, 128, 260, 1, 90),
     (1, 700, 4, 48, 650, 1, 300),     # index_dim not a multiple of 64
+    (1, 1100, 8, 32, 1100, 1, 1100),  # more than 1024 slots a row: the scatter reads them in place
 ])
 def test_random_selection(B, S, H, D, Skv, ratio, topk):
     g = np.random.default_rng(S + H)
